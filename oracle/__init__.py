@@ -1,0 +1,29 @@
+"""fp64 CPU oracle for exact attention — TEST INFRASTRUCTURE ONLY.
+
+This package is the slow, obviously-correct statement of what the GPU path
+computes.  Only the test-suite, ``__graft_entry__.smoke()`` and ``bench.py``'s
+CPU-baseline / reference arm may import it.  The CUDA library never calls it,
+and it imports nothing from the CUDA package: the two share no code.
+
+Sources (web pages, cited by title and section):
+  * "Advanced attention mechanisms – II" (Aryan Das): sections "Why?",
+    "Flash Attention", "Tiling" (steps 1–3), "Softmax stabiliser",
+    "Incremental / online softmax".
+  * "Fast attention kernels and operator fusion accelerate AI models":
+    section "FlashAttention-style attention and Paged Attention".
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
+force, closed forms, a library routine and invariants the mathematics fixes.
+No function is "parity unpinned".
+"""
+
+from .definitions import (  # noqa: F401
+    attention,
+    attention_online,
+    combine_partials,
+    decode_paged,
+    gather_paged_keys,
+    score_matrix,
+    softmax_probs,
+    split_partials,
+)

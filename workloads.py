@@ -1,0 +1,109 @@
+"""Seeded synthetic inputs shared by the tests, ``bench.py`` and the oracle checks.
+
+This module only draws random numbers and lays them out: it holds none of
+the attention arithmetic, so both the CUDA path and the fp64 oracle can be
+fed from it without sharing any code with each other.
+
+Every tensor is drawn in fp32 from ``torch.Generator().manual_seed(seed)``
+on the CPU and rounded to bf16 (round-to-nearest-even); the oracle consumes
+the exact bf16 values (upcast to fp64) and the GPU gets the same bits.
+
+The shapes mirror the pages' workloads: GPT-2-sized heads ("Advanced
+attention mechanisms – II", section "Flash Attention"), a Qwen2.5-1.5B-style
+GQA layer and block_size = 16 paged decode ("Fast attention kernels and
+operator fusion accelerate AI models", section "FlashAttention-style
+attention and Paged Attention").  No model weights or datasets are used.
+"""
+
+import math
+
+import torch
+
+BLOCK_SIZE = 16
+
+# name -> parameters of the five workloads
+PREFILL_CONFIGS = {
+    "tiny": dict(B=1, Hq=2, Hkv=2, N=256, d=64, std=1.0, key_offset=False, seed=0),
+    "gpt2_small": dict(B=8, Hq=12, Hkv=12, N=1024, d=64, std=1.0, key_offset=False, seed=1),
+    "qwen_gqa_prefill": dict(B=4, Hq=12, Hkv=2, N=4096, d=128, std=1.0, key_offset=False, seed=2),
+    "long_context": dict(B=1, Hq=16, Hkv=16, N=16384, d=128, std=0.5, key_offset=True, seed=3),
+}
+DECODE_CONFIGS = {
+    "paged_decode": dict(num_seqs=64, Hq=12, Hkv=2, d=128, len_lo=128, len_hi=4096, seed=4),
+}
+
+
+def _randn(gen, shape, std=1.0):
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    if std != 1.0:
+        x = x * std
+    return x
+
+
+def prefill_inputs(B, Hq, Hkv, N, d, seed, std=1.0, key_offset=False):
+    """q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 (CPU), entries ~ N(0, std^2).
+
+    With ``key_offset`` every key row j of every head gets one extra
+    N(0, 1) draw added to all of its d components (a per-row offset that
+    widens the range of the logits, as in the long-context workload).
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    q = _randn(gen, (B, Hq, N, d), std)
+    k = _randn(gen, (B, Hkv, N, d), std)
+    v = _randn(gen, (B, Hkv, N, d), std)
+    if key_offset:
+        k = k + _randn(gen, (B, Hkv, N, 1))
+    return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+
+
+def default_scale(d):
+    """1/sqrt(d) rounded to fp32 — the value handed to both sides."""
+    return float(torch.tensor(1.0 / math.sqrt(d), dtype=torch.float32))
+
+
+def decode_inputs(num_seqs, Hq, Hkv, d, seed, len_lo=128, len_hi=4096,
+                  seq_lens=None, block_size=BLOCK_SIZE, permute=True,
+                  nan_unused=True, max_blocks_per_seq=None, spare_blocks=0):
+    """Paged-cache decode inputs.
+
+    seq_lens ~ U{len_lo..len_hi} (inclusive) unless given.  The physical
+    pool holds exactly sum ceil(L/16) blocks (+ ``spare_blocks`` unused
+    ones); each sequence's table row is a consecutive slice of one random
+    permutation of the pool (identity when ``permute`` is False), padded
+    with -1.  Cache slots past a sequence's length in its last block are
+    filled with NaN (``nan_unused``) so that reading them would show.
+
+    Returns a dict of CPU tensors: q [S,Hq,d] bf16, k_cache / v_cache
+    [num_blocks,Hkv,block_size,d] bf16, block_table [S,max_blocks] int32,
+    seq_lens [S] int32.
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    if seq_lens is None:
+        seq_lens = torch.randint(len_lo, len_hi + 1, (num_seqs,), generator=gen)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int64)
+    nblk = [(int(L) + block_size - 1) // block_size for L in seq_lens]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(1, (len_hi + block_size - 1) // block_size, max(nblk + [1]))
+    num_blocks = sum(nblk) + int(spare_blocks)
+    num_blocks = max(num_blocks, 1)
+    if permute:
+        perm = torch.randperm(num_blocks, generator=gen)
+    else:
+        perm = torch.arange(num_blocks)
+    table = torch.full((num_seqs, max_blocks_per_seq), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    q = _randn(gen, (num_seqs, Hq, d)).to(torch.bfloat16)
+    k_cache = _randn(gen, (num_blocks, Hkv, block_size, d)).to(torch.bfloat16)
+    v_cache = _randn(gen, (num_blocks, Hkv, block_size, d)).to(torch.bfloat16)
+    if nan_unused:
+        for b, L in enumerate(seq_lens.tolist()):
+            if L % block_size:
+                phys = int(table[b, L // block_size])
+                k_cache[phys, :, L % block_size:] = float("nan")
+                v_cache[phys, :, L % block_size:] = float("nan")
+    return dict(q=q, k_cache=k_cache, v_cache=v_cache, block_table=table,
+                seq_lens=seq_lens.to(torch.int32), block_size=block_size,
+                max_blocks_per_seq=max_blocks_per_seq, num_blocks=num_blocks)
