@@ -1,0 +1,423 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  attn_fwd           Qwen2.5-1.5B-style GQA prefill: B=4, Hq=12, Hkv=2,
+                     N=4096, d=128, causal, bf16 (one launch)
+  attn_decode_paged  64 sequences, Hq=12, Hkv=2, d=128, block_size 16,
+                     lengths U[128, 4096], permuted block table (two launches)
+Printed (rank 0, one JSON line): fwd TFLOP/s as `value` (causal flops
+4*B*Hq*N^2*d/2 over the forward kernel's CUDA-event time), the decode's HBM
+GB/s (algorithmic bytes over its kernels' time) under "decode", rooflines
+against the measured peaks, the same metric end to end through the public
+API with pinned host buffers ("e2e"), the fp64 oracle on host cores
+("cpu_baseline"), and the SM clocks sampled while the GPU ran.
+
+L2: three input sets (about 0.75 GB in total, above the 129 MB L2) are used
+in rotation, so no step finds its inputs in L2 from the previous step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+Under torchrun (N > 1) every rank runs its own replica (its own seeds) with
+no data exchange; times are max-reduced over ranks (weak scaling).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (bf16, causal) & % tensor peak; paged-decode HBM GB/s"
+FWD_CFG = "qwen_gqa_prefill"
+DEC_CFG = "paged_decode"
+NSETS = 3
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
+# ncu summaries (profiles/); None until captured for the current kernels.
+TRAFFIC_FWD = None
+TRAFFIC_DEC = None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def fwd_flops(c):
+    return 4.0 * c["B"] * c["Hq"] * c["N"] * c["N"] * c["d"] / 2.0
+
+
+def decode_bytes(inp, Hq, Hkv, d):
+    total_L = int(inp["seq_lens"].to(torch.int64).sum())
+    S = inp["q"].shape[0]
+    kv = total_L * Hkv * d * 2 * 2                 # K and V rows addressed, bf16
+    qo = S * Hq * d * 2 * 2                        # q in, o out
+    lse = S * Hq * 4
+    meta = S * inp["block_table"].shape[1] * 4 + S * 4
+    return kv + qo + lse + meta
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.rows = []
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                self.rows.append(dict(t=ts + frac, sm=float(parts[1]), sm_max=float(parts[2]),
+                                      power=parts[3], active=parts[4], hw=parts[5], hwt=parts[6],
+                                      swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+
+    def summary(self, t0, t1):
+        inside = [r for r in self.rows if t0 <= r["t"] <= t1]
+        window = "timed region"
+        if not inside:
+            # the timed region was shorter than the sampling period: use the
+            # samples of the busy period around it (warm-up + timed steps)
+            inside = [r for r in self.rows if t0 - 1.0 <= r["t"] <= t1 + 1.0]
+            window = "busy period around the timed region"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        reasons = set()
+        for r in inside:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["sm_max"] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------- CPU arm
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(target_s=12.0):
+    """Time the fp64 oracle (as it stands) on whole (b, head) slices of the
+    forward workload until about `target_s` seconds of CPU work are done."""
+    import oracle
+
+    c = workloads.PREFILL_CONFIGS[FWD_CFG]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
+    scale = workloads.default_scale(c["d"])
+    qn, kn, vn = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    G = c["Hq"] // c["Hkv"]
+    heads = 0
+    t0 = time.perf_counter()
+    while heads < c["B"] * c["Hq"]:
+        b, h = divmod(heads, c["Hq"])
+        oracle.attention(qn[b:b + 1, h:h + 1], kn[b:b + 1, h // G:h // G + 1],
+                         vn[b:b + 1, h // G:h // G + 1], scale, True)
+        heads += 1
+        if time.perf_counter() - t0 >= target_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 4.0 * heads * c["N"] * c["N"] * c["d"] / 2.0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "%d of %d (batch, query head) slices of the %s workload (full causal rows), "
+                      "fp64 numpy, %.1f s" % (heads, c["B"] * c["Hq"], FWD_CFG, dt)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+
+    c = workloads.PREFILL_CONFIGS[FWD_CFG]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
+    scale = workloads.default_scale(c["d"])
+    qn, kn, vn = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    G = c["Hq"] // c["Hkv"]
+
+    def step(i):  # one (batch, head) slice of the forward workload per step
+        b, h = divmod(i % (c["B"] * c["Hq"]), c["Hq"])
+        oracle.attention(qn[b:b + 1, h:h + 1], kn[b:b + 1, h // G:h // G + 1],
+                         vn[b:b + 1, h // G:h // G + 1], scale, True)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * args.steps * c["N"] * c["N"] * c["d"] / 2.0
+    value = flops / dt / 1e12
+    sample = ("one (batch, query head) slice of the %s workload per step (N=%d, d=%d, causal), "
+              "fp64 numpy oracle" % (FWD_CFG, c["N"], c["d"]))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": FWD_CFG + " (B4 Hq12 Hkv2 N4096 d128 causal)", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def build_sets(rank, device):
+    import exact_attention_47_gb300 as attn
+
+    c = workloads.PREFILL_CONFIGS[FWD_CFG]
+    dc = workloads.DECODE_CONFIGS[DEC_CFG]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"],
+                                       c["seed"] + 1000 * rank)
+    dec = workloads.decode_inputs(dc["num_seqs"], dc["Hq"], dc["Hkv"], dc["d"],
+                                  dc["seed"] + 1000 * rank, dc["len_lo"], dc["len_hi"])
+    host = dict(q=q, k=k, v=v, dec=dec)
+    sets = []
+    ws_bytes = attn.attn_decode_paged_workspace_size(dc["num_seqs"], dc["Hq"], dc["d"],
+                                                     dec["max_blocks_per_seq"])
+    for _ in range(NSETS):
+        s = dict(q=q.to(device), k=k.to(device), v=v.to(device),
+                 o=torch.empty(q.shape, dtype=torch.bfloat16, device=device),
+                 lse=torch.empty(q.shape[:3], dtype=torch.float32, device=device),
+                 dq=dec["q"].to(device), kc=dec["k_cache"].to(device), vc=dec["v_cache"].to(device),
+                 bt=dec["block_table"].to(device), sl=dec["seq_lens"].to(device),
+                 do=torch.empty(dec["q"].shape, dtype=torch.bfloat16, device=device),
+                 dlse=torch.empty(dec["q"].shape[:2], dtype=torch.float32, device=device),
+                 ws=torch.empty(ws_bytes, dtype=torch.uint8, device=device))
+        sets.append(s)
+    return c, dc, host, sets
+
+
+def run_gpu(args, rank, world, local_rank):
+    import exact_attention_47_gb300 as attn
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    c, dc, host, sets = build_sets(rank, device)
+    scale_f = workloads.default_scale(c["d"])
+    scale_d = workloads.default_scale(dc["d"])
+    flops = fwd_flops(c)
+    dbytes = decode_bytes(host["dec"], dc["Hq"], dc["Hkv"], dc["d"])
+    stream = torch.cuda.current_stream()
+
+    def fwd(s):
+        attn.attn_fwd(s["q"], s["k"], s["v"], causal=True, scale=scale_f, o=s["o"], lse=s["lse"])
+
+    def dec(s):
+        attn.attn_decode_paged(s["dq"], s["kc"], s["vc"], s["bt"], s["sl"], scale=scale_d,
+                               o=s["do"], lse=s["dlse"], workspace=s["ws"])
+
+    clock = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ
+                         else os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
+    clock.start()
+    for i in range(args.warmup):
+        s = sets[i % NSETS]
+        fwd(s)
+        dec(s)
+    torch.cuda.synchronize()
+    if attn.device_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(K):
+        s = sets[i % NSETS]
+        ev[i][0].record(stream)
+        fwd(s)
+        ev[i][1].record(stream)
+        dec(s)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    if attn.device_status() != 0:
+        raise RuntimeError("device status flags set during the timed steps")
+
+    # ---- end to end through the public API with pinned host buffers
+    h_q, h_k, h_v = (host[x].pin_memory() for x in ("q", "k", "v"))
+    hd = host["dec"]
+    h_dq, h_bt, h_sl = hd["q"].pin_memory(), hd["block_table"].pin_memory(), hd["seq_lens"].pin_memory()
+    h_o = torch.empty(h_q.shape, dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty(h_q.shape[:3], dtype=torch.float32).pin_memory()
+    h_do = torch.empty(h_dq.shape, dtype=torch.bfloat16).pin_memory()
+    h_dlse = torch.empty(h_dq.shape[:2], dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_dq, h_bt, h_sl))
+    d2h = sum(t.numel() * t.element_size() for t in (h_o, h_lse, h_do, h_dlse))
+
+    def e2e_step(s):
+        s["q"].copy_(h_q, non_blocking=True)
+        s["k"].copy_(h_k, non_blocking=True)
+        s["v"].copy_(h_v, non_blocking=True)
+        s["dq"].copy_(h_dq, non_blocking=True)
+        s["bt"].copy_(h_bt, non_blocking=True)
+        s["sl"].copy_(h_sl, non_blocking=True)
+        fwd(s)
+        dec(s)
+        h_o.copy_(s["o"], non_blocking=True)
+        h_lse.copy_(s["lse"], non_blocking=True)
+        h_do.copy_(s["do"], non_blocking=True)
+        h_dlse.copy_(s["dlse"], non_blocking=True)
+
+    for i in range(max(1, min(args.warmup, 3))):
+        e2e_step(sets[i % NSETS])
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        e2e_step(sets[i % NSETS])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+    clock.stop()
+
+    # ---- max over ranks
+    fwd_sum = sum(fwd_ms)
+    dec_sum = sum(dec_ms)
+    vals = torch.tensor([total_ms, fwd_sum, dec_sum, e2e_ms], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    total_ms, fwd_sum, dec_sum, e2e_ms = vals.tolist()
+
+    if rank == 0:
+        pk, pk_kind = peaks()
+        fwd_avg_s = fwd_sum / K / 1e3
+        dec_avg_s = dec_sum / K / 1e3
+        tflops = world * flops / fwd_avg_s / 1e12
+        gbs = world * dbytes / dec_avg_s / 1e9
+        achieved_fwd = flops / fwd_avg_s / 1e12
+        achieved_dec = dbytes / dec_avg_s / 1e9
+        line = {
+            "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "%s (B4 Hq12 Hkv2 N4096 d128 causal) + %s (64 seqs, Hq12 "
+                                   "Hkv2 d128, block_size 16, L~U[128,4096])" % (FWD_CFG, DEC_CFG),
+                       "l2": "3 input sets rotated (~0.75 GB > 129 MB L2); no flush",
+                       "flop_convention": "4*B*Hq*N^2*d/2 (causal)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved_fwd,
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved_fwd / pk["bf16_tflops"], "traffic": TRAFFIC_FWD,
+                         "kernel": "attn_fwd_sm103_kernel<128,causal>",
+                         "peak_kind": pk_kind + " burst bf16 (cuBLAS)",
+                         "fwd_ms_mean": fwd_sum / K, "fwd_ms_median": statistics.median(fwd_ms)},
+            "decode": {"value": gbs, "unit": "GB/s", "ms_mean": dec_sum / K,
+                       "ms_median": statistics.median(dec_ms), "bytes_per_step": dbytes,
+                       "roofline": {"bound": "hbm", "achieved": achieved_dec,
+                                    "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                    "frac": achieved_dec / pk["hbm_gbs"], "traffic": TRAFFIC_DEC,
+                                    "kernel": "attn_decode_paged_kernel<128> + combine",
+                                    "peak_kind": pk_kind + " copy bandwidth"}},
+            "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "note": "fwd flops over the whole step: pinned h2d of q,k,v and of the "
+                            "decode query/table/lengths, both ops, d2h of all outputs"},
+            "gpu_launches": 3 * K,
+            "clocks": clock.summary(wall0, wall1),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_sample(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_gpu(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,26 @@
+"""GB300 (sm_103a) exact attention: tiled online-softmax prefill and paged-KV decode.
+
+The compute lives in ``lib/libattn47_sm103.so`` (hand-written CUDA, C-ABI
+declared in ``include/attn47.h``); this package is its Python binding.
+Importing the package does not load the library; the first call does, and
+raises if it is not built.  Build with ``exact_attention_47_gb300.build_lib``.
+"""
+
+from ._binding import (  # noqa: F401
+    ATTN_DEV_BAD_BLOCK,
+    ATTN_DEV_BAD_SEQLEN,
+    ATTN_DEV_TIMEOUT,
+    BLOCK_SIZE,
+    AttnError,
+    abi_version,
+    attn_decode_paged,
+    attn_decode_paged_workspace_size,
+    attn_fwd,
+    device_status,
+    library_path,
+    load_library,
+    selftest_wait_timeout,
+    set_decode_split_blocks,
+    set_wait_timeout_ns,
+    status_string,
+)

@@ -1,0 +1,210 @@
+"""ctypes binding of ``libattn47_sm103.so`` (argument marshalling only).
+
+Every function here checks tensor properties the C-ABI cannot see (device,
+dtype, contiguity, shapes), allocates outputs with torch when the caller
+passes none, and forwards raw device pointers plus the current torch CUDA
+stream to the C entry point of the same name.  All arithmetic runs in the
+library's CUDA kernels; there is no other code path.  If the library is not
+built, every call raises ``RuntimeError``.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from .build_lib import LIB_PATH
+
+ATTN_OK = 0
+ATTN_DEV_TIMEOUT = 0x1
+ATTN_DEV_BAD_BLOCK = 0x2
+ATTN_DEV_BAD_SEQLEN = 0x4
+BLOCK_SIZE = 16
+
+# C entry points and their signatures (mirrors include/attn47.h)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "attn_decode_paged_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                               _P, _P, _P, ctypes.c_size_t, _P]),
+    "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
+    "attn_set_decode_split_blocks": (None, [_I]),
+    "attn_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_abi_version": (_I, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero attn_status_t from the library."""
+
+    def __init__(self, func, status, message):
+        self.status = status
+        super().__init__("%s failed: %s: %s" % (func, status_string(status), message))
+
+
+def library_path():
+    return LIB_PATH
+
+
+def load_library(path=None):
+    """Load (once) and return the ctypes handle of the CUDA library."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "CUDA library %s is not built; run `python -c \"import __graft_entry__ as g; g.build()\"` "
+            "(there is no CPU fallback)" % path)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status):
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _check(func, status):
+    if status != ATTN_OK:
+        raise AttnError(func, status, load_library().attn_last_error().decode())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need_cuda(name, t, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None, return_lse=True, stream=None):
+    """Exact attention forward.  q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 on the GPU.
+
+    Returns (o, lse): o [B,Hq,N,d] bf16, lse [B,Hq,N] fp32 (None when
+    ``return_lse`` is False and no ``lse`` buffer is given).
+    """
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+        if t.dim() != 4:
+            raise ValueError("%s must be 4-D [B, H, N, d]" % name)
+    B, Hq, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need_cuda("o", o, torch.bfloat16)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need_cuda("lse", lse, torch.float32)
+        if tuple(lse.shape) != (B, Hq, N):
+            raise ValueError("lse must be [B, Hq, N]")
+    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                      1 if causal else 0, float(scale), _stream_handle(stream))
+    _check("attn_fwd", st)
+    return o, lse
+
+
+def attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq):
+    return int(load_library().attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq))
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, o=None, lse=None,
+                      workspace=None, return_lse=True, stream=None):
+    """Paged-KV decode.  q [S,Hq,d]; caches [num_blocks,Hkv,16,d] bf16;
+    block_table [S,max_blocks] int32; seq_lens [S] int32 (all on the GPU).
+
+    Returns (o [S,Hq,d] bf16, lse [S,Hq] fp32 or None).
+    """
+    lib = load_library()
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("k_cache", k_cache, torch.bfloat16)
+    _need_cuda("v_cache", v_cache, torch.bfloat16)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("seq_lens", seq_lens, torch.int32)
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [S,Hq,d] and caches [num_blocks,Hkv,block_size,d]")
+    S, Hq, d = q.shape
+    num_blocks, Hkv, block_size, dk = k_cache.shape
+    if dk != d:
+        raise ValueError("cache head dim differs from q")
+    if block_table.dim() != 2 or block_table.shape[0] != S or tuple(seq_lens.shape) != (S,):
+        raise ValueError("block_table must be [S, max_blocks] and seq_lens [S]")
+    max_blocks = block_table.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need_cuda("o", o, torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
+    need = attn_decode_paged_workspace_size(S, Hq, d, max_blocks)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                               _ptr(seq_lens), S, Hq, Hkv, d, block_size, max_blocks, num_blocks,
+                               float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check("attn_decode_paged", st)
+    return o, lse
+
+
+def device_status(stream=None):
+    """Read and clear the device status word (ATTN_DEV_* bits)."""
+    flags = ctypes.c_uint(0)
+    _check("attn_get_device_status",
+           load_library().attn_get_device_status(_stream_handle(stream), ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def set_wait_timeout_ns(ns):
+    load_library().attn_set_wait_timeout_ns(int(ns))
+
+
+def set_decode_split_blocks(blocks):
+    load_library().attn_set_decode_split_blocks(int(blocks))
+
+
+def selftest_wait_timeout(timeout_ns, stream=None):
+    flags = ctypes.c_uint(0)
+    _check("attn_selftest_wait_timeout",
+           load_library().attn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream),
+                                                     ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def abi_version():
+    return int(load_library().attn_abi_version())

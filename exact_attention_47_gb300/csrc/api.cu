@@ -1,0 +1,333 @@
+// C-ABI of the exact-attention library: host-side validation, device check,
+// TMA descriptor encoding and launches.  See include/attn47.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attn47.h"
+#include "decode_sm103.h"
+#include "fwd_sm103.h"
+#include "ptx.cuh"
+
+// Per-device error word written by the kernels (ATTN_DEV_* bits).
+__device__ unsigned int g_attn47_status;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+attn_status_t fail(attn_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+unsigned long long g_timeout_ns = 1000000000ull;
+int g_decode_split_blocks = 0;  // 0 = choose per call
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool checked = false;
+  bool usable = false;
+  int sms = 0;
+  unsigned int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device, checked once: compute capability 10.3, status word address.
+attn_status_t current_device(DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_DEVICE, "no usable CUDA device: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    d.sms = sms;
+    if (major != 10 || minor != 3) {
+      d.checked = true;
+      d.usable = false;
+      return fail(ATTN_ERR_DEVICE, "device %d is compute capability %d.%d; this library is built "
+                  "for sm_103a (10.3) only", dev, major, minor);
+    }
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_attn47_status);
+    if (e != cudaSuccess)
+      return fail(ATTN_ERR_DEVICE, "status word unavailable: %s", cudaGetErrorString(e));
+    d.status = static_cast<unsigned int*>(addr);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(ATTN_ERR_DEVICE, "driver entry point cuTensorMapEncodeTiled not found");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.usable = true;
+    d.checked = true;
+  }
+  if (!d.usable) return fail(ATTN_ERR_DEVICE, "device %d is not a compute capability 10.3 GPU", dev);
+  *out = &d;
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
+
+// bf16 tensor map over `rank` dims (innermost first), 64-column boxes,
+// 128-byte swizzle, zero fill out of bounds.
+attn_status_t encode_bf16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                          const cuuint32_t* box) {
+  cuuint64_t strides[4];
+  cuuint64_t acc = dims[0] * 2;
+  for (int i = 1; i < rank; ++i) {
+    strides[i - 1] = acc;
+    acc *= dims[i];
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
+attn_status_t launch_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "%s launch failed: %s", what, cudaGetErrorString(e));
+  g_last_error[0] = '\0';
+  return ATTN_OK;
+}
+
+int decode_split_blocks(int num_seqs, int Hkv, int max_blocks, int sms) {
+  if (g_decode_split_blocks > 0) return g_decode_split_blocks;
+  // Largest split that still gives >= 8 CTAs per SM in the worst case.
+  for (int sb = attn47::kMaxSplitBlocks; sb > attn47::kMinSplitBlocks; sb /= 2) {
+    const long long units =
+        static_cast<long long>(num_seqs) * Hkv * ((max_blocks + sb - 1) / sb);
+    if (units >= 8LL * sms) return sb;
+  }
+  return attn47::kMinSplitBlocks;
+}
+
+__global__ void selftest_wait_kernel(unsigned int* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    attn47::mbar_init(attn47::smem_addr(&bar), 1);
+    abort_flag = 0;
+    attn47::fence_mbar_init();
+  }
+  __syncwarp();
+  const attn47::WaitCtl wc{&abort_flag, status, timeout_ns};
+  // Nothing arrives on `bar`: the wait must give up after timeout_ns.
+  attn47::mbar_wait_warp(attn47::smem_addr(&bar), 0, wc);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_abi_version(void) { return ATTN47_ABI_VERSION; }
+
+const char* attn_last_error(void) { return g_last_error; }
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE";
+    case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns < 1000ull ? 1000ull : ns; }
+
+void attn_set_decode_split_blocks(int blocks) {
+  if (blocks <= 0) {
+    g_decode_split_blocks = 0;
+    return;
+  }
+  int b = blocks < attn47::kMinSplitBlocks ? attn47::kMinSplitBlocks : blocks;
+  g_decode_split_blocks = b > attn47::kMaxSplitBlocks ? attn47::kMaxSplitBlocks : b;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
+  if (B < 0 || N < 0 || Hq < 1 || Hkv < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy B >= 0, N >= 0, Hq >= 1, Hkv >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (B == 0 || N == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!q || !k || !v || !o) return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (static_cast<long long>(B) * Hq * tiles > 0x7fffffffLL || static_cast<long long>(B) * Hq > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  const cuuint32_t rows = static_cast<cuuint32_t>(attn47::fwd_box_rows());
+  const cuuint32_t box[3] = {64, rows, 1};
+  const cuuint64_t dq[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                            static_cast<cuuint64_t>(B) * Hq};
+  const cuuint64_t dkv[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                             static_cast<cuuint64_t>(B) * Hkv};
+  alignas(64) CUtensorMap tq, tk, tv;
+  if ((st = encode_bf16(&tq, q, 3, dq, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tk, k, 3, dkv, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tv, v, 3, dkv, box)) != ATTN_OK) return st;
+
+  attn47::FwdLaunch a;
+  a.tq = &tq;
+  a.tk = &tk;
+  a.tv = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_fwd_sm103(a), "attn_fwd");
+}
+
+size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq) {
+  if (num_seqs <= 0 || Hq <= 0 || d <= 0 || max_blocks_per_seq <= 0) return 0;
+  const int max_splits = (max_blocks_per_seq + attn47::kMinSplitBlocks - 1) / attn47::kMinSplitBlocks;
+  return attn47::decode_workspace_floats(num_seqs, Hq, d, max_splits) * sizeof(float);
+}
+
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+                                int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, void* o, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "sizes must satisfy num_seqs >= 0, Hq, Hkv, max_blocks_per_seq, num_blocks >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (block_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (Hq / Hkv > 16) return fail(ATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16 not supported", Hq / Hkv);
+  if (static_cast<long long>(num_blocks) * Hkv * block_size >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "KV pool too large (num_blocks * Hkv * 16 >= 2^31)");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  if (num_seqs == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !workspace)
+    return fail(ATTN_ERR_INVALID_ARG, "q, caches, block_table, seq_lens, o, workspace must be non-null");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
+    return fail(ATTN_ERR_INVALID_ARG, "q, caches, o and workspace must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "block_table, seq_lens and lse must be 4-byte aligned");
+  const size_t need = attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq);
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
+                              static_cast<cuuint64_t>(num_blocks) * Hkv * block_size};
+  alignas(64) CUtensorMap tk, tv;
+  if ((st = encode_bf16(&tk, k_cache, 2, dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tv, v_cache, 2, dims, box)) != ATTN_OK) return st;
+
+  attn47::DecLaunch a;
+  a.tk = &tk;
+  a.tv = &tv;
+  a.q = q;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.lse = lse;
+  a.workspace = static_cast<float*>(workspace);
+  a.num_seqs = num_seqs;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.split_blocks = decode_split_blocks(num_seqs, Hkv, max_blocks_per_seq, dev->sms);
+  a.max_splits = (max_blocks_per_seq + a.split_blocks - 1) / a.split_blocks;
+  a.scale = scale;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_decode_sm103(a), "attn_decode_paged");
+}
+
+attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {
+  if (!flags_out) return fail(ATTN_ERR_INVALID_ARG, "flags_out must be non-null");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, dev->status, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev->status, 0, sizeof(unsigned int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_DEVICE, "status read failed: %s", cudaGetErrorString(e));
+  *flags_out = host;
+  g_last_error[0] = '\0';
+  return ATTN_OK;
+}
+
+attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream,
+                                         unsigned int* flags_out) {
+  if (!flags_out) return fail(ATTN_ERR_INVALID_ARG, "flags_out must be non-null");
+  if (timeout_ns > 10000000000ull) return fail(ATTN_ERR_INVALID_ARG, "timeout above 10 s");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  selftest_wait_kernel<<<1, 32, 0, s>>>(dev->status, timeout_ns);
+  st = launch_result(cudaGetLastError(), "selftest");
+  if (st != ATTN_OK) return st;
+  return attn_get_device_status(stream, flags_out);
+}
+
+}  // extern "C"

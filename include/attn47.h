@@ -1,0 +1,180 @@
+/*
+ * attn47.h — C-ABI of the GB300 (sm_103a) exact-attention library
+ * (libattn47_sm103.so).
+ *
+ * Two operations, both bf16 in / fp32 accumulate:
+ *
+ *  attn_fwd           softmax(scale * Q K^T + causal mask) V for a whole
+ *                     sequence (prefill), computed tile by tile with the
+ *                     running-max / running-sum softmax so the N x N score
+ *                     matrix never reaches global memory.  Defined by
+ *                     "Advanced attention mechanisms – II" (Aryan Das),
+ *                     sections "Why?" (the matmul -> mask -> softmax -> V
+ *                     pipeline whose result this is), "Flash Attention"
+ *                     (only the output goes back to HBM), "Tiling" steps 1-3,
+ *                     "Softmax stabiliser" and "Incremental / online softmax";
+ *                     and by "Fast attention kernels and operator fusion
+ *                     accelerate AI models", section "FlashAttention-style
+ *                     attention and Paged Attention" (blocks of Q, K, V;
+ *                     softmax statistics and outputs kept on chip).
+ *
+ *  attn_decode_paged  one query token per sequence attending to all of its
+ *                     cached keys, where the KV cache is stored in fixed-size
+ *                     blocks of 16 token slots and a block table maps each
+ *                     logical position to a physical block.  Defined by "Fast
+ *                     attention kernels and operator fusion accelerate AI
+ *                     models", section "FlashAttention-style attention and
+ *                     Paged Attention" (paged cache, block table, per-position
+ *                     translation; block_size = 16 in its worked example).
+ *
+ * Conventions shared by every call
+ *  - Pointers are DEVICE pointers of the current CUDA device unless stated.
+ *    The caller owns every buffer and the stream; the library allocates no
+ *    device memory and performs no host<->device copy.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on that stream.
+ *  - Every argument is validated on the host before anything is launched.
+ *    An unsupported shape, head size, block size or device returns an error;
+ *    there is never a fallback to another implementation ("Fast attention
+ *    kernels ...", same section: forcing a fixed backend fails when it does
+ *    not support the inputs or the hardware, and the serving engine reports
+ *    an incompatible backend at initialisation).
+ *  - Only devices of compute capability 10.3 (GB300, sm_103a) are accepted.
+ *  - Problems found on the device (a wait that ran out of time, a block-table
+ *    entry outside the pool, a sequence length outside the table) set bits in
+ *    a per-device status word instead of trapping; read and clear it with
+ *    attn_get_device_status().
+ *  - GQA: query head h reads KV head h / (Hq / Hkv) (contiguous groups; MQA is
+ *    Hkv = 1, MHA is Hkv = Hq).
+ *  - LSE is the natural logarithm of sum_j exp(scale * q . k_j) over the keys
+ *    the row may see.
+ */
+#ifndef ATTN47_H_
+#define ATTN47_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN47_ABI_VERSION 1
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad scale, Hq % Hkv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented: d not in {64,128}, block_size != 16,
+                                Hq/Hkv > 16 (decode) */
+  ATTN_ERR_DEVICE = 3,       /* no CUDA device, or not compute capability 10.3 */
+  ATTN_ERR_LAUNCH = 4,       /* the CUDA runtime rejected the launch; see attn_last_error() */
+  ATTN_ERR_WORKSPACE = 5     /* workspace smaller than attn_decode_paged_workspace_size() */
+} attn_status_t;
+
+/* Bits of the device status word (attn_get_device_status). */
+#define ATTN_DEV_TIMEOUT 0x1u    /* a kernel wait exceeded its time limit; outputs invalid */
+#define ATTN_DEV_BAD_BLOCK 0x2u  /* a block-table entry was outside [0, num_blocks); that block
+                                    was skipped */
+#define ATTN_DEV_BAD_SEQLEN 0x4u /* a seq_lens entry was < 0 or > max_blocks_per_seq*block_size;
+                                    it was clamped into range */
+
+/*
+ * attn_fwd — exact attention forward (prefill).
+ *
+ *  q    [B, Hq,  N, d] bf16, contiguous, 16-byte aligned
+ *  k, v [B, Hkv, N, d] bf16, contiguous, 16-byte aligned
+ *  o    [B, Hq,  N, d] bf16 (written), 16-byte aligned
+ *  lse  [B, Hq,  N]    fp32 (written) or NULL to skip it
+ *  causal != 0: query i sees keys j <= i (Nq = Nk = N); 0: every key.
+ *  scale: multiplies q . k before the softmax (finite, > 0), e.g. 1/sqrt(d).
+ *  d must be 64 or 128; Hq % Hkv == 0; B, Hq, Hkv >= 1; N >= 0.
+ *  B == 0 or N == 0 is an empty problem: returns ATTN_OK, launches nothing.
+ *  Writes only o and lse.  Deterministic (no atomics).
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_decode_paged_workspace_size — bytes of device workspace that
+ * attn_decode_paged needs for these sizes (fp32 partial results of the
+ * key-range splits).  0 for an empty problem.
+ */
+size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq);
+
+/*
+ * attn_decode_paged — one query token per sequence over a paged KV cache.
+ *
+ *  q            [num_seqs, Hq, d] bf16, 16-byte aligned
+ *  k_cache,
+ *  v_cache      [num_blocks, Hkv, block_size, d] bf16, 16-byte aligned
+ *  block_table  [num_seqs, max_blocks_per_seq] int32: logical block i of
+ *               sequence b lives in physical block block_table[b][i]; entries
+ *               past ceil(seq_lens[b] / block_size) are never read
+ *  seq_lens     [num_seqs] int32 (device): number of cached tokens of each
+ *               sequence; the query is that sequence's last token and
+ *               attends to all of them.  seq_lens[b] == 0 gives o = 0 and
+ *               lse = -inf for that sequence.  Slots past seq_lens[b] in the
+ *               last block are never used, whatever they hold.
+ *  o            [num_seqs, Hq, d] bf16 (written)
+ *  lse          [num_seqs, Hq] fp32 (written) or NULL
+ *  workspace    >= attn_decode_paged_workspace_size(...) bytes, 16-byte
+ *               aligned; contents on entry are ignored
+ *  block_size must be 16; d must be 64 or 128; Hq % Hkv == 0 and
+ *  Hq / Hkv <= 16; num_blocks * Hkv * 16 < 2^31.
+ *  num_seqs == 0 is an empty problem: returns ATTN_OK, launches nothing.
+ *  Launches two kernels (split decode, then merge).  Deterministic.
+ */
+attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+                                int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, void* o, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * attn_get_device_status — synchronises `stream`, copies the current
+ * device's status word (ATTN_DEV_* bits) to *flags_out (host pointer) and
+ * clears it.  Returns ATTN_ERR_DEVICE if the device is unusable.
+ */
+attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out);
+
+/*
+ * attn_set_wait_timeout_ns — time limit of every wait inside the kernels
+ * (default 1e9 ns = 1 s); after it a kernel sets ATTN_DEV_TIMEOUT, lets its
+ * in-flight copies land, releases its tensor memory and returns.  Applies to
+ * later launches from this process.  Values < 1000 are raised to 1000.
+ */
+void attn_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * attn_set_decode_split_blocks — number of logical blocks (8..32) that one
+ * decode work unit covers; 0 (the default) lets each call choose from the
+ * problem size and the SM count.  Values are clamped to [8, 32].  Any choice
+ * gives the same result up to fp32 rounding order; it only changes how the
+ * keys are spread over the SMs.  Applies to later calls from this process.
+ */
+void attn_set_decode_split_blocks(int blocks);
+
+/*
+ * attn_selftest_wait_timeout — launches a one-warp kernel that waits on a
+ * shared-memory barrier that nothing will ever complete, with the given time
+ * limit, so the bounded-wait path can be tested without hanging or faulting
+ * the GPU.  Synchronises `stream`; on return *flags_out holds the status
+ * word (ATTN_DEV_TIMEOUT expected), which is then cleared.
+ */
+attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream,
+                                         unsigned int* flags_out);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_status_string(attn_status_t s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* attn_last_error(void);
+
+/* ATTN47_ABI_VERSION of the loaded library. */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN47_H_ */

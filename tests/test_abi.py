@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every function ``include/attn47.h``
+declares, and rejects bad arguments on the host before touching a device.
+
+These run without a GPU: no call here launches a kernel.  Pointers passed
+to calls that must fail validation are never dereferenced.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_47_gb300 as attn
+from exact_attention_47_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn47.h")
+
+OK, INVALID, UNSUPPORTED, DEVICE, LAUNCH, WORKSPACE = 0, 1, 2, 3, 4, 5
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced on these paths
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(attn.library_path()):
+        import __graft_entry__
+        __graft_entry__.build()
+    return attn.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("attn_fwd", "attn_decode_paged", "attn_decode_paged_workspace_size",
+                     "attn_get_device_status", "attn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _binding._SIGS, "binding lacks " + name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert attn.abi_version() == 1
+    assert attn.status_string(0) == "ATTN_OK"
+    assert attn.status_string(5) == "ATTN_ERR_WORKSPACE"
+
+
+def _fwd(lib, B=1, Hq=2, Hkv=2, N=16, d=64, causal=1, scale=0.125, q=FAKE, o=FAKE):
+    return lib.attn_fwd(q, FAKE, FAKE, o, None, B, Hq, Hkv, N, d, causal, scale, None)
+
+
+def test_fwd_host_validation(lib):
+    assert _fwd(lib, d=96) == UNSUPPORTED
+    assert _fwd(lib, Hq=3, Hkv=2) == INVALID
+    assert _fwd(lib, N=-1) == INVALID
+    assert _fwd(lib, scale=0.0) == INVALID
+    assert _fwd(lib, scale=float("nan")) == INVALID
+    assert _fwd(lib, q=ctypes.c_void_p(0x10008)) == INVALID      # misaligned
+    assert _fwd(lib, o=ctypes.c_void_p(0)) == INVALID            # null output
+    assert "aligned" in lib.attn_last_error().decode() or "null" in lib.attn_last_error().decode()
+    assert _fwd(lib, B=0) == OK                                  # empty problem
+    assert _fwd(lib, N=0) == OK
+
+
+def _dec(lib, S=2, Hq=12, Hkv=2, d=128, bs=16, mb=4, nb=8, ws_bytes=None, ws=FAKE):
+    need = lib.attn_decode_paged_workspace_size(S, Hq, d, mb)
+    if ws_bytes is None:
+        ws_bytes = need
+    return lib.attn_decode_paged(FAKE, FAKE, FAKE, FAKE, FAKE, S, Hq, Hkv, d, bs, mb, nb, 0.1,
+                                 FAKE, None, ws, ws_bytes, None)
+
+
+def test_decode_host_validation(lib):
+    assert _dec(lib, bs=8) == UNSUPPORTED
+    assert _dec(lib, d=80) == UNSUPPORTED
+    assert _dec(lib, Hq=34, Hkv=2) == UNSUPPORTED               # group of 17
+    assert _dec(lib, Hq=12, Hkv=5) == INVALID
+    assert _dec(lib, ws_bytes=16) == WORKSPACE
+    assert _dec(lib, ws=ctypes.c_void_p(0)) == INVALID
+    assert _dec(lib, S=0) == OK
+
+
+def test_workspace_size_formula(lib):
+    # fp32 partial O (d floats) + max and sum per (seq, head, split of >= 8 blocks)
+    assert lib.attn_decode_paged_workspace_size(64, 12, 128, 256) == 64 * 12 * 32 * 130 * 4
+    assert lib.attn_decode_paged_workspace_size(0, 12, 128, 256) == 0
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _binding.load_library(str(tmp_path / "missing.so"))

@@ -1,0 +1,164 @@
+"""GPU parity of attn_decode_paged (through the C-ABI) against the fp64 oracle.
+
+Covers the full paged-decode workload (64 sequences, Hq 12, Hkv 2, d 128,
+lengths U[128, 4096], block_size 16, permuted block table) on every output,
+the ragged lengths around block edges, empty sequences, NaN in unused slots,
+paging invariances, and the device-side checks of bad table entries.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_47_gb300 as attn
+import oracle
+import workloads
+from parity import assert_attn_close, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def to_dev(inp):
+    return {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def run(inp, scale, **kw):
+    d = to_dev(inp)
+    o, lse = attn.attn_decode_paged(d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                    d["seq_lens"], scale=scale, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def ref(inp, scale):
+    return oracle.decode_paged(inp["q"].double().numpy(), inp["k_cache"].double().numpy(),
+                               inp["v_cache"].double().numpy(), inp["block_table"].numpy(),
+                               inp["seq_lens"].numpy(), scale)
+
+
+def test_paged_decode_config_all_outputs():
+    c = workloads.DECODE_CONFIGS["paged_decode"]
+    inp = workloads.decode_inputs(c["num_seqs"], c["Hq"], c["Hkv"], c["d"], c["seed"],
+                                  c["len_lo"], c["len_hi"])
+    scale = workloads.default_scale(c["d"])
+    o, lse = run(inp, scale)
+    assert attn.device_status() == 0
+    assert_attn_close(o, lse, *ref(inp, scale), what="paged_decode")
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(12, 2, 128), (8, 8, 64), (16, 1, 128), (6, 3, 64)])
+def test_ragged_lengths(Hq, Hkv, d):
+    lens = [1, 15, 16, 17, 31, 32, 33, 100, 255, 256, 257, 700, 4096]
+    inp = workloads.decode_inputs(len(lens), Hq, Hkv, d, seed=20 + Hq + d, seq_lens=lens,
+                                  len_hi=4096)
+    scale = workloads.default_scale(d)
+    o, lse = run(inp, scale)
+    assert attn.device_status() == 0
+    assert_attn_close(o, lse, *ref(inp, scale), what="ragged")
+
+
+def test_empty_sequence_gives_zero_and_minus_inf():
+    inp = workloads.decode_inputs(4, 12, 2, 128, seed=21, seq_lens=[0, 5, 0, 40], len_hi=64)
+    o, lse = run(inp, 0.1)
+    o_ref, lse_ref = ref(inp, 0.1)
+    assert_attn_close(o, lse, o_ref, lse_ref, what="empty")
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_nan_in_unused_slots_does_not_leak():
+    inp = workloads.decode_inputs(6, 12, 2, 128, seed=22, seq_lens=[1, 7, 17, 30, 49, 63],
+                                  len_hi=64, nan_unused=True)
+    o, lse = run(inp, 0.1)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    assert_attn_close(o, lse, *ref(inp, 0.1), what="nan slots")
+
+
+def test_permuted_pool_gives_identical_bits():
+    inp = workloads.decode_inputs(8, 12, 2, 128, seed=23, len_lo=1, len_hi=600)
+    o1, l1 = run(inp, 0.1)
+    nb = inp["k_cache"].shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(5))
+    k2 = torch.empty_like(inp["k_cache"]); v2 = torch.empty_like(inp["v_cache"])
+    k2[perm] = inp["k_cache"]; v2[perm] = inp["v_cache"]
+    t = inp["block_table"].long()
+    t2 = torch.where(t >= 0, perm[t.clamp(min=0)], t).to(torch.int32)
+    inp2 = dict(inp, k_cache=k2, v_cache=v2, block_table=t2)
+    o2, l2 = run(inp2, 0.1)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_equals_prefill_last_row():
+    """Paging changes only where keys live: decode == last row of the causal
+    forward over the same keys laid out contiguously (both on the GPU)."""
+    L, Hq, Hkv, d = 333, 12, 2, 128
+    inp = workloads.decode_inputs(1, Hq, Hkv, d, seed=24, seq_lens=[L], len_hi=512)
+    o_dec, l_dec = run(inp, 0.088)
+    kc, vc, table = inp["k_cache"], inp["v_cache"], inp["block_table"][0]
+    pos = torch.arange(L)
+    phys = table[pos // 16].long()
+    k = kc[phys, :, pos % 16].permute(1, 0, 2).unsqueeze(0).contiguous()   # [1,Hkv,L,d]
+    v = vc[phys, :, pos % 16].permute(1, 0, 2).unsqueeze(0).contiguous()
+    q = torch.zeros(1, Hq, L, d, dtype=torch.bfloat16)
+    q[0, :, L - 1] = inp["q"][0]
+    o_fwd, l_fwd = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, scale=0.088)
+    torch.cuda.synchronize()
+    assert (o_fwd[0, :, L - 1].float() - o_dec[0].float()).abs().max().item() <= 2e-2
+    assert (l_fwd[0, :, L - 1] - l_dec[0]).abs().max().item() <= 1e-3
+
+
+@pytest.mark.parametrize("split", [8, 16, 32])
+def test_split_size_does_not_change_the_result(split):
+    inp = workloads.decode_inputs(5, 12, 2, 128, seed=25, len_lo=1, len_hi=2000)
+    try:
+        attn.set_decode_split_blocks(split)
+        o, lse = run(inp, 0.1)
+    finally:
+        attn.set_decode_split_blocks(0)
+    assert_attn_close(o, lse, *ref(inp, 0.1), what="split %d" % split)
+
+
+def test_deterministic():
+    inp = workloads.decode_inputs(9, 12, 2, 128, seed=26, len_lo=1, len_hi=3000)
+    o1, l1 = run(inp, 0.1)
+    o2, l2 = run(inp, 0.1)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bad_block_entry_is_reported_not_faulted():
+    inp = workloads.decode_inputs(3, 12, 2, 128, seed=27, seq_lens=[40, 40, 40], len_hi=64)
+    attn.device_status()  # clear
+    bad = inp["block_table"].clone()
+    bad[1, 1] = inp["k_cache"].shape[0] + 100        # outside the pool
+    o, lse = run(dict(inp, block_table=bad), 0.1)
+    assert attn.device_status() & attn.ATTN_DEV_BAD_BLOCK
+    # the other sequences are untouched
+    o_ref, lse_ref = ref(inp, 0.1)
+    assert_attn_close(to64(o)[[0, 2]], to64(lse)[[0, 2]], o_ref[[0, 2]], lse_ref[[0, 2]])
+
+
+def test_bad_seq_len_is_clamped_and_reported():
+    inp = workloads.decode_inputs(2, 12, 2, 128, seed=28, seq_lens=[32, 20], len_hi=32,
+                                  max_blocks_per_seq=2)
+    attn.device_status()
+    sl = inp["seq_lens"].clone()
+    sl[1] = 1000                                     # more than 2 blocks of 16
+    run(dict(inp, seq_lens=sl), 0.1)
+    assert attn.device_status() & attn.ATTN_DEV_BAD_SEQLEN
+
+
+def test_small_workspace_is_rejected():
+    inp = workloads.decode_inputs(2, 12, 2, 128, seed=29, len_hi=64)
+    ws = torch.empty(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(attn.AttnError, match="WORKSPACE"):
+        run(inp, 0.1, workspace=ws)
+
+
+def test_bounded_wait_times_out_and_reports():
+    """A barrier nothing completes: the kernel gives up after 20 ms, sets
+    the timeout bit and returns; the context stays usable."""
+    flags = attn.selftest_wait_timeout(20_000_000)
+    assert flags & attn.ATTN_DEV_TIMEOUT
+    x = torch.ones(4, device=DEV)
+    assert float(x.sum()) == 4.0
+    assert attn.device_status() == 0

@@ -1,0 +1,124 @@
+"""GPU parity of attn_fwd (through the C-ABI) against the fp64 oracle.
+
+Small cases are compared on every output element; the full-size workloads
+(GPT-2-sized heads, Qwen-style GQA prefill, long context) in the launch
+configuration the bench times, on all rows (GPT-2) or on sampled rows,
+which the oracle computes one by one (rows are independent).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_47_gb300 as attn
+import oracle
+import workloads
+from parity import assert_attn_close, sample_rows, to64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run(q, k, v, causal, scale):
+    o, lse = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0
+    return o, lse
+
+
+def ref(q, k, v, causal, scale, rows=None):
+    return oracle.attention(q.double().numpy(), k.double().numpy(), v.double().numpy(), scale,
+                            causal, rows=rows)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_config(causal):
+    c = workloads.PREFILL_CONFIGS["tiny"]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
+    scale = workloads.default_scale(c["d"])
+    o, lse = run(q, k, v, causal, scale)
+    assert_attn_close(o, lse, *ref(q, k, v, causal, scale), what="tiny")
+
+
+SMALL = [  # B, Hq, Hkv, N, d  — ragged tails, several tiles, GQA / MQA
+    (1, 2, 2, 1, 64), (1, 2, 1, 17, 64), (2, 3, 3, 129, 128), (1, 4, 2, 255, 128),
+    (1, 6, 1, 300, 64), (2, 2, 2, 1000, 128), (1, 12, 2, 513, 128), (2, 6, 6, 384, 64),
+    (1, 1, 1, 128, 128), (1, 8, 4, 640, 64),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B%dHq%dHkv%dN%dd%d" % s)
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_shapes(shape, causal):
+    B, Hq, Hkv, N, d = shape
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, N, d, seed=100 + N + d)
+    scale = workloads.default_scale(d)
+    o, lse = run(q, k, v, causal, scale)
+    assert_attn_close(o, lse, *ref(q, k, v, causal, scale), what=str(shape))
+
+
+@pytest.mark.parametrize("scale", [0.02, 0.3, 1.0])
+def test_scales_and_wide_logits(scale):
+    q, k, v = workloads.prefill_inputs(1, 4, 2, 384, 128, seed=11, std=1.5, key_offset=True)
+    o, lse = run(q, k, v, True, scale)
+    assert_attn_close(o, lse, *ref(q, k, v, True, scale), what="scale %g" % scale)
+
+
+def test_gpt2_small_config_all_rows():
+    c = workloads.PREFILL_CONFIGS["gpt2_small"]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
+    scale = workloads.default_scale(c["d"])
+    o, lse = run(q, k, v, True, scale)
+    assert_attn_close(o, lse, *ref(q, k, v, True, scale), what="gpt2")
+
+
+@pytest.mark.parametrize("name", ["qwen_gqa_prefill", "long_context"])
+def test_full_size_sampled_rows(name):
+    c = workloads.PREFILL_CONFIGS[name]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"],
+                                       std=c["std"], key_offset=c["key_offset"])
+    scale = workloads.default_scale(c["d"])
+    o, lse = run(q, k, v, True, scale)
+    rows = sample_rows(c["N"], 97)
+    o_ref, lse_ref = ref(q, k, v, True, scale, rows=rows)
+    assert_attn_close(to64(o)[:, :, rows], to64(lse)[:, :, rows], o_ref, lse_ref, what=name)
+
+
+def test_causal_row_zero_is_exactly_v0():
+    q, k, v = workloads.prefill_inputs(2, 4, 2, 300, 128, seed=12)
+    o, _ = run(q, k, v, True, 0.09)
+    vv = v.repeat_interleave(2, dim=1)
+    assert torch.equal(o[:, :, 0].cpu(), vv[:, :, 0])
+
+
+def test_constant_v_gives_constant_output():
+    q, k, v = workloads.prefill_inputs(1, 2, 2, 333, 64, seed=13)
+    c = torch.randn(64).to(torch.bfloat16)
+    v = c.expand_as(v).contiguous()
+    for causal in (False, True):
+        o, _ = run(q, k, v, causal, 0.125)
+        err = (o.cpu().float() - c.float()).abs().max().item()
+        assert err <= 2e-2
+
+
+def test_deterministic_and_lse_optional():
+    q, k, v = workloads.prefill_inputs(1, 6, 2, 700, 128, seed=14)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1, l1 = attn.attn_fwd(qd, kd, vd, causal=True)
+    o2, l2 = attn.attn_fwd(qd, kd, vd, causal=True)
+    o3, l3 = attn.attn_fwd(qd, kd, vd, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    assert l3 is None
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+def test_empty_sequence_is_a_no_op():
+    q = torch.empty(1, 2, 0, 64, dtype=torch.bfloat16, device=DEV)
+    o, lse = attn.attn_fwd(q, q, q, causal=True)
+    assert o.numel() == 0 and lse.numel() == 0
+
+
+def test_unsupported_head_dim_raises():
+    q = torch.zeros(1, 1, 8, 96, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(attn.AttnError, match="UNSUPPORTED"):
+        attn.attn_fwd(q, q, q)
