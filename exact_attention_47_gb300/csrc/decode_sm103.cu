@@ -328,6 +328,8 @@ struct CombineParams {
 };
 
 // One warp per (sequence, query head): exact merge of the split partials.
+// Lane s holds split s's (max, sum); the weights come from warp reductions
+// and every split's partial row is loaded before any is accumulated.
 template <int D>
 __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -340,18 +342,40 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
   const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.max_splits;
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ws_ml[(base + s) * 2]);
+  for (int s0 = 0; s0 < nsplit; s0 += 32)
+    if (s0 + lane < nsplit) M = fmaxf(M, p.ws_ml[(base + s0 + lane) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[D / 32];
 #pragma unroll
   for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
   float lsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float wt = ex2(p.ws_ml[(base + s) * 2] - M);
-      lsum += wt * p.ws_ml[(base + s) * 2 + 1];
-      const float* src = p.ws_o + (base + s) * D;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+      const int cnt = min(32, nsplit - s0);
+      float w = 0.f, lw = 0.f;
+      if (lane < cnt) {
+        w = ex2(p.ws_ml[(base + s0 + lane) * 2] - M);
+        lw = w * p.ws_ml[(base + s0 + lane) * 2 + 1];
+      }
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) acc[e] += wt * src[lane + 32 * e];
+      for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+      lsum += lw;
+      for (int s = 0; s < cnt; s += 4) {
+        float v[4][D / 32], ws[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          ws[u] = __shfl_sync(0xffffffffu, w, min(s + u, 31));
+          const float* src = p.ws_o + (base + s0 + min(s + u, cnt - 1)) * D;
+#pragma unroll
+          for (int e = 0; e < D / 32; ++e) v[u][e] = src[lane + 32 * e];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (s + u < cnt)
+#pragma unroll
+            for (int e = 0; e < D / 32; ++e) acc[e] += ws[u] * v[u][e];
+      }
     }
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;

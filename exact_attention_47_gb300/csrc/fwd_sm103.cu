@@ -7,16 +7,26 @@
 // "Fast attention kernels and operator fusion accelerate AI models", section
 // "FlashAttention-style attention and Paged Attention").
 //
-// One CTA owns one 128-row query tile of one (batch, query head) and streams
-// the 128-row K/V tiles of its KV head:
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into TMEM (fp32),
-//               O += P_j V_j into TMEM; owns the TMEM allocation
-//   warps 2..5  softmax: one thread per query row (= TMEM lane); masks,
-//               running max/sum in the exp2 domain, rescales O when the max
-//               moves, writes P_j (bf16) to shared memory; final O / l and LSE
-// S is double-buffered in TMEM so S_{j+1} runs on the tensor core while the
-// softmax warps work on S_j.
+// One CTA owns a 256-row query block of one (batch, query head), split into
+// two 128-row tiles A and B that share every K/V tile of the KV head:
+//   warps 0-3   softmax of tile A, one thread per query row (= TMEM lane)
+//   warps 4-7   softmax of tile B
+//   warp 8      TMA producer: Q_A, Q_B once, then K_j / V_j into a stage ring
+//   warp 9      MMA issuer (one thread) and owner of the TMEM allocation
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+// Tensor memory: S_A, S_B (128 fp32 columns each), O_A, O_B (d columns
+// each).  After reading S_X, the softmax writes P_X (bf16, two per column)
+// over the first 64 columns of S_X and the MMA reads it from there (A
+// operand in TMEM), so P never touches shared memory.  The tensor core runs
+// ... PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ... in issue order, so while one
+// warpgroup computes exponentials the tensor core works on the other tile,
+// and the completion of S_X(j+1) also proves PV_X(j) has finished, which
+// makes O_X and the P_X columns safe to touch again.
+//
+// The stabiliser m of a row ("Softmax stabiliser") is only moved when the
+// tile maximum exceeds it by more than 2^8 (in the exp2 domain), so O and l
+// are rescaled rarely; exponents stay <= 8, numerators <= 256, and the final
+// O / l and LSE are the same function of the same stabiliser.
 #include <cuda_runtime.h>
 
 #include "fwd_sm103.h"
@@ -25,35 +35,45 @@
 namespace attn47 {
 namespace {
 
-constexpr int kBM = 128;           // query rows per tile (= TMEM lanes)
-constexpr int kBN = 128;           // keys per tile
-constexpr int kThreads = 192;      // 6 warps
+constexpr int kBM = 128;            // rows per query tile (= TMEM lanes)
+constexpr int kBN = 128;            // keys per K/V tile
+constexpr int kTiles = 2;           // query tiles per CTA
+constexpr int kRowsPerCta = kBM * kTiles;
+constexpr int kThreads = 384;       // 2 softmax warpgroups + 1 producer/MMA warpgroup
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+// Launched at 168 registers a thread (384 x 168 = 64512); the softmax
+// warpgroups then take 224 and the producer/MMA warpgroup keeps 56:
+// 256 x 224 + 128 x 56 = 64512, and per sub-partition 224 + 224 + 56 = 504
+// = 3 x 168, so the increase never waits for registers nobody frees.
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsOther = 56;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kTau = 8.0f;        // lazy-rescale threshold, log2 units
 
 template <int D>
 struct FwdLayout {
   static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
-  static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kKVBytes = kBN * D * 2;
-  static constexpr int kQChunk = kBM * 128;              // one 64-column box of the Q tile
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kQTile = kBM * D * 2;
+  static constexpr int kKV = kBN * D * 2;
+  static constexpr int kQChunk = kBM * 128;              // one 64-column box of a Q tile
   static constexpr int kKVChunk = kBN * 128;
-  static constexpr int kPChunk = kBM * 128;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffP + kBM * kBN * 2;
+  static constexpr int kOffK = kOffQ + kTiles * kQTile;
+  static constexpr int kOffV = kOffK + kStages * kKV;
+  static constexpr int kOffBar = kOffV + kStages * kKV;
   static constexpr int kSmem = kOffBar + 512 + 1024;     // barriers + alignment slack
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
 
 struct FwdBarriers {
   uint64_t q_full;
-  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, mma_final;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t mma_final;
   uint32_t tmem_base;
   int abort;
 };
@@ -61,7 +81,7 @@ struct FwdBarriers {
 struct FwdParams {
   void* o;
   float* lse;
-  int N, Hq, Hkv, group, num_q_tiles, bh_total;
+  int N, Hq, Hkv, group, num_q_blocks, bh_total;
   float scale_log2;
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -80,20 +100,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_addr(smem + L::kOffQ);
   const uint32_t sK = smem_addr(smem + L::kOffK);
   const uint32_t sV = smem_addr(smem + L::kOffV);
-  const uint32_t sP = smem_addr(smem + L::kOffP);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heaviest (last, for causal) query tiles first across the whole grid.
-  const int tile = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x) / p.bh_total;
+  // Heaviest (last, for causal) query blocks first across the whole grid.
+  const int qblk = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x) / p.bh_total;
   const int bh = static_cast<int>(blockIdx.x) % p.bh_total;
-  const int h = bh % p.Hq;
-  const int b = bh / p.Hq;
   const int zq = bh;                                   // b * Hq + h
-  const int zkv = b * p.Hkv + h / p.group;
-  const int kv_tiles_total = (p.N + kBN - 1) / kBN;
-  const int n_kv = CAUSAL ? min(tile + 1, kv_tiles_total) : kv_tiles_total;
+  const int zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+  const int kv_total = (p.N + kBN - 1) / kBN;
+  // K/V tiles each query tile needs; the diagonal tile of tile X is 2*qblk + X.
+  const int nA = CAUSAL ? min(2 * qblk + 1, kv_total) : kv_total;
+  const int nB = CAUSAL ? min(2 * qblk + 2, kv_total) : kv_total;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bar->q_full), 1);
@@ -103,17 +122,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bar->k_empty[s]), 1);
       mbar_init(smem_addr(&bar->v_empty[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&bar->s_full[s]), 1);
-      mbar_init(smem_addr(&bar->s_free[s]), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_addr(&bar->s_full[x]), 1);
+      mbar_init(smem_addr(&bar->p_full[x]), 4);
+      mbar_init(smem_addr(&bar->o_done[x]), 1);
     }
-    mbar_init(smem_addr(&bar->p_full), 4);
-    mbar_init(smem_addr(&bar->o_done), 1);
     mbar_init(smem_addr(&bar->mma_final), 1);
     bar->abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -122,32 +140,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
-
-  if (warp == 0) {
+  if (warp >= 8) {
+  regs_decrease<kRegsOther>();
+  if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       const uint32_t qf = smem_addr(&bar->q_full);
-      mbar_arrive_expect_tx(qf, L::kQBytes);
-      for (int c = 0; c < L::kChunks; ++c)
-        tma_load_3d(sQ + c * L::kQChunk, &tq, qf, c * 64, tile * kBM, zq);
+      mbar_arrive_expect_tx(qf, kTiles * L::kQTile);
+      for (int x = 0; x < kTiles; ++x)
+        for (int c = 0; c < L::kChunks; ++c)
+          tma_load_3d(sQ + x * L::kQTile + c * L::kQChunk, &tq, qf, c * 64,
+                      qblk * kRowsPerCta + x * kBM, zq);
       int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
+      for (int j = 0; j < nB; ++j) {
         const int st = j % L::kStages;
         const uint32_t ph = (j / L::kStages) & 1;
         if (!mbar_wait(smem_addr(&bar->k_empty[st]), ph ^ 1, wc)) break;
         const uint32_t kf = smem_addr(&bar->k_full[st]);
-        mbar_arrive_expect_tx(kf, L::kKVBytes);
+        mbar_arrive_expect_tx(kf, L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sK + st * L::kKVBytes + c * L::kKVChunk, &tk, kf, c * 64, j * kBN, zkv);
+          tma_load_3d(sK + st * L::kKV + c * L::kKVChunk, &tk, kf, c * 64, j * kBN, zkv);
         ++k_issued;
         if (!mbar_wait(smem_addr(&bar->v_empty[st]), ph ^ 1, wc)) break;
         const uint32_t vf = smem_addr(&bar->v_full[st]);
-        mbar_arrive_expect_tx(vf, L::kKVBytes);
+        mbar_arrive_expect_tx(vf, L::kKV);
         for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + st * L::kKVBytes + c * L::kKVChunk, &tv, vf, c * 64, j * kBN, zkv);
+          tma_load_3d(sV + st * L::kKV + c * L::kKVChunk, &tv, vf, c * 64, j * kBN, zkv);
         ++v_issued;
       }
       // Every copy issued must have landed before the CTA may exit.
@@ -159,84 +180,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nv) mbar_wait(smem_addr(&bar->v_full[st]), (nv - 1) & 1, wc, true);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // --------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
-      bool ok = mbar_wait(smem_addr(&bar->q_full), 0, wc);
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i % L::kStages;
-        if (!mbar_wait(smem_addr(&bar->p_full), i & 1, wc)) return false;
-        if (!mbar_wait(smem_addr(&bar->v_full[st]), (i / L::kStages) & 1, wc)) return false;
+      auto issue_s = [&](int x, int j) -> bool {
+        const int st = j % L::kStages;
+        if (!mbar_wait(smem_addr(&bar->k_full[st]), (j / L::kStages) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t vbase = sV + st * L::kKVBytes;
+        const uint32_t qbase = sQ + x * L::kQTile;
+        const uint32_t kbase = sK + st * L::kKV;
+        const uint32_t dS = tmem + (x ? L::kColS1 : L::kColS0);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A = P (K-major, 128-byte swizzle), B = V (MN-major: d contiguous).
-          const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * L::kPChunk + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kKVChunk, 1024);
-          umma_ss(tmem + kColO, ad, bd, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(qbase + (kk >> 2) * L::kQChunk + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kKVChunk + (kk & 3) * 32, 16, 1024);
+          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(smem_addr(&bar->o_done));
-        umma_commit(smem_addr(&bar->v_empty[st]));
+        umma_commit(smem_addr(&bar->s_full[x]));
         return true;
       };
-      if (ok) {
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int st = j % L::kStages;
+        if (!mbar_wait(smem_addr(&bar->p_full[x]), j & 1, wc)) return false;
+        if (!mbar_wait(smem_addr(&bar->v_full[st]), (j / L::kStages) & 1, wc)) return false;
         tc_fence_after();
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const int sb = j & 1;
-          const int st = j % L::kStages;
-          if (!mbar_wait(smem_addr(&bar->s_free[sb]), ((j >> 1) & 1) ^ 1, wc)) { ok = false; break; }
-          if (!mbar_wait(smem_addr(&bar->k_full[st]), (j / L::kStages) & 1, wc)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t kbase = sK + st * L::kKVBytes;
-          const uint32_t dS = tmem + (sb ? kColS1 : kColS0);
+        const uint32_t vbase = sV + st * L::kKV;
+        const uint32_t aP = tmem + (x ? L::kColS1 : L::kColS0);
+        const uint32_t dO = tmem + (x ? L::kColO1 : L::kColO0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * L::kQChunk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kKVChunk + (kk & 3) * 32, 16, 1024);
-            umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(smem_addr(&bar->s_full[sb]));
-          umma_commit(smem_addr(&bar->k_empty[st]));
-          if (j > 0) ok = issue_pv(j - 1);
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // A = P from TMEM (8 columns = 16 keys per step), B = V (MN-major).
+          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kKVChunk, 1024);
+          umma_ts(dO, aP + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        if (ok) issue_pv(n_kv - 1);
+        return true;
+      };
+      bool ok = mbar_wait(smem_addr(&bar->q_full), 0, wc);
+      if (ok) ok = issue_s(0, 0);
+      if (ok) ok = issue_s(1, 0);
+      if (ok) umma_commit(smem_addr(&bar->k_empty[0]));
+      for (int j = 0; j < nB && ok; ++j) {
+        const int st = j % L::kStages;
+        if (j < nA) {
+          if (!(ok = issue_pv(0, j))) break;
+          if (j == nA - 1) umma_commit(smem_addr(&bar->o_done[0]));
+        }
+        if (j + 1 < nA && !(ok = issue_s(0, j + 1))) break;
+        if (!(ok = issue_pv(1, j))) break;
+        umma_commit(smem_addr(&bar->v_empty[st]));
+        if (j == nB - 1) umma_commit(smem_addr(&bar->o_done[1]));
+        if (j + 1 < nB) {
+          if (!(ok = issue_s(1, j + 1))) break;
+          umma_commit(smem_addr(&bar->k_empty[(j + 1) % L::kStages]));
+        }
       }
       // All issued MMAs must retire before TMEM is released.
       umma_commit(smem_addr(&bar->mma_final));
       mbar_wait(smem_addr(&bar->mma_final), 0, wc, true);
     }
+  }
+    // Each role ends on the same named barrier, so the register-split
+    // branches never merge back; then the MMA warp frees the TMEM.
+    tc_fence_before();
+    named_barrier_sync(1, kThreads);
+    if (warp == kWarpMma) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
   } else {
+    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
+    const int x = warp >> 2;                       // query tile of this warpgroup
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;           // row within the tile = TMEM lane
-    const int qrow = tile * kBM + row;
+    const int qrow = qblk * kRowsPerCta + x * kBM + row;
+    const int n_kv = x ? nB : nA;
+    const int diag = 2 * qblk + x;                 // causal: the tile holding key == row
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colS = x ? L::kColS1 : L::kColS0;
+    const uint32_t colO = x ? L::kColO1 : L::kColO0;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;                           // running max, exp2 domain
-    float l = 0.f;                                 // running denominator
+    float m = 0.f;                                 // stabiliser in use (exp2 domain)
+    float l = 0.f;                                 // denominator relative to m (fp32 terms)
+    float lr = 0.f;                                // same, bf16-rounded terms
     bool ok = true;
-    const uint32_t prow = sP + (row >> 3) * 1024 + (row & 7) * 128;
 
     for (int j = 0; j < n_kv; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_warp(smem_addr(&bar->s_full[sb]), (j >> 1) & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_addr(&bar->s_full[x]), j & 1, wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
-      const uint32_t cs = tl + (sb ? kColS1 : kColS0);
-      ATTN47_TMEM_LD32(cs + 0, r0);
-      ATTN47_TMEM_LD32(cs + 32, r1);
-      ATTN47_TMEM_LD32(cs + 64, r2);
-      ATTN47_TMEM_LD32(cs + 96, r3);
+      ATTN47_TMEM_LD32(tl + colS + 0, r0);
+      ATTN47_TMEM_LD32(tl + colS + 32, r1);
+      ATTN47_TMEM_LD32(tl + colS + 64, r2);
+      ATTN47_TMEM_LD32(tl + colS + 96, r3);
       ATTN47_TMEM_LD_WAIT(r0);
       ATTN47_TMEM_LD_WAIT(r1);
       ATTN47_TMEM_LD_WAIT(r2);
       ATTN47_TMEM_LD_WAIT(r3);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->s_free[sb]));
 
       float s[128];
 #pragma unroll
@@ -247,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s[96 + c] = __uint_as_float(r3[c]);
       }
       const int kbase = j * kBN;
-      const bool need_mask = CAUSAL ? (kbase + kBN - 1 > tile * kBM) : (kbase + kBN > p.N);
+      const bool need_mask = CAUSAL ? (j == diag) : (kbase + kBN > p.N);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
@@ -259,63 +301,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = s[0];
 #pragma unroll
       for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);
-      float rs = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, -m_use));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, -m_use));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      m = m_new;
-
-      // PV_{j-1} must have finished reading P and writing O.
-      if (j > 0) {
-        if (!mbar_wait_warp(smem_addr(&bar->o_done), (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      const float mt = mx * sl2;
+      if (j == 0) {
+        m = (mt == -INFINITY) ? 0.f : mt;
+      } else {
+        const bool need = mt > m + kTau;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mt : m;
+          const float alpha = ex2(m - m_new);
+          l *= alpha;
+          lr *= alpha;
+          m = m_new;
+          // O_X holds PV_X(0..j-1), complete since S_X(j) completed after it.
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
-            ATTN47_TMEM_LD32(tl + kColO + c0, o);
+            ATTN47_TMEM_LD32(tl + colO + c0, o);
             ATTN47_TMEM_LD_WAIT(o);
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            ATTN47_TMEM_ST32(tl + kColO + c0, o);
+            ATTN47_TMEM_ST32(tl + colO + c0, o);
           }
-          tmem_st_wait();
         }
       }
-      // P row -> shared memory in the K-major 128-byte-swizzled layout.
+      // Two denominators: `lr` sums the bf16-rounded numerators that P V
+      // uses, so O / lr weights every value row by exactly the factor it got;
+      // `l` sums the fp32 numerators and gives the LSE.
+      const float nm = -m;
+      float rs0 = 0.f, rs1 = 0.f, re0 = 0.f, re1 = 0.f;
+      uint32_t pk0[32], pk1[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t addr = prow + (c >> 3) * L::kPChunk + (((c & 7) ^ (row & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]),
-                     "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(s[2 * c], sl2, nm));
+        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, nm));
+        const uint32_t w = pack_bf16x2(p0, p1);
+        re0 += p0;
+        re1 += p1;
+        rs0 += __uint_as_float(w << 16);
+        rs1 += __uint_as_float(w & 0xffff0000u);
+        pk0[c] = w;
       }
-      fence_proxy_async_smem();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(s[64 + 2 * c], sl2, nm));
+        const float p1 = ex2(fmaf(s[64 + 2 * c + 1], sl2, nm));
+        const uint32_t w = pack_bf16x2(p0, p1);
+        re0 += p0;
+        re1 += p1;
+        rs0 += __uint_as_float(w << 16);
+        rs1 += __uint_as_float(w & 0xffff0000u);
+        pk1[c] = w;
+      }
+      lr += rs0 + rs1;
+      l += re0 + re1;
+      // P_X over the first 64 columns of S_X (keys 2c, 2c+1 in column c).
+      ATTN47_TMEM_ST32(tl + colS + 0, pk0);
+      ATTN47_TMEM_ST32(tl + colS + 32, pk1);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full[x]));
     }
 
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait_warp(smem_addr(&bar->o_done), (n_kv - 1) & 1, wc)) {
+    if (ok && mbar_wait_warp(smem_addr(&bar->o_done[x]), 0, wc)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / lr;
       const bool in_range = qrow < p.N;
       __nv_bfloat16* orow =
           reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(zq) * p.N + qrow) * D;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        ATTN47_TMEM_LD32(tl + kColO + c0, o);
+        ATTN47_TMEM_LD32(tl + colO + c0, o);
         ATTN47_TMEM_LD_WAIT(o);
         uint32_t w[16];
 #pragma unroll
@@ -331,13 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (in_range && p.lse != nullptr)
         p.lse[static_cast<size_t>(zq) * p.N + qrow] = (m + __log2f(l)) * kLn2;
     }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tc_fence_before();
+    named_barrier_sync(1, kThreads);
   }
 }
 
@@ -354,12 +407,12 @@ cudaError_t launch_t(const FwdLaunch& a) {
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
   p.group = a.Hq / a.Hkv;
-  p.num_q_tiles = (a.N + kBM - 1) / kBM;
+  p.num_q_blocks = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   p.bh_total = a.B * a.Hq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  const unsigned grid = static_cast<unsigned>(p.num_q_tiles) * static_cast<unsigned>(p.bh_total);
+  const unsigned grid = static_cast<unsigned>(p.num_q_blocks) * static_cast<unsigned>(p.bh_total);
   kern<<<grid, kThreads, L::kSmem, a.stream>>>(*a.tq, *a.tk, *a.tv, p);
   return cudaGetLastError();
 }

@@ -74,7 +74,7 @@ struct WaitCtl {
 // Returns false (and records kDevTimeout) once `timeout_ns` has passed, or
 // at once when another role of the CTA already aborted (unless
 // `ignore_abort`, used while draining copies that are still in flight).
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                                    volatile int* abort, unsigned int* status,
                                                    unsigned long long timeout_ns,
                                                    bool ignore_abort) {
@@ -102,6 +102,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 // proceeds when all lanes saw the phase complete.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
+}
+
+// Per-warpgroup register budget changes (all four warps of a warpgroup).
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Named CTA barrier (id 1..15) over `count` threads; threads may reach it
+// from different places in the code.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ----------------------------------------------------------------------- TMA
@@ -156,6 +172,17 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(tmem) * B(smem desc): A is read from tensor memory (one row
+// per lane, two consecutive 16-bit K elements per 32-bit column).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.

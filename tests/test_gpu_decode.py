@@ -148,7 +148,7 @@ def test_bad_seq_len_is_clamped_and_reported():
 
 
 def test_small_workspace_is_rejected():
-    inp = workloads.decode_inputs(2, 12, 2, 128, seed=29, len_hi=64)
+    inp = workloads.decode_inputs(2, 12, 2, 128, seed=29, len_lo=1, len_hi=64)
     ws = torch.empty(64, dtype=torch.uint8, device=DEV)
     with pytest.raises(attn.AttnError, match="WORKSPACE"):
         run(inp, 0.1, workspace=ws)

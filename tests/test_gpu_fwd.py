@@ -59,7 +59,11 @@ def test_small_shapes(shape, causal):
 
 @pytest.mark.parametrize("scale", [0.02, 0.3, 1.0])
 def test_scales_and_wide_logits(scale):
-    q, k, v = workloads.prefill_inputs(1, 4, 2, 384, 128, seed=11, std=1.5, key_offset=True)
+    """Wide, peaky logits (q, k with std 1.5 and per-key offsets).  V keeps
+    unit scale as in the workloads: the absolute bound is about outputs of
+    order one (a bf16 ulp of |o| in [4, 8) alone is 0.031)."""
+    q, k, _ = workloads.prefill_inputs(1, 4, 2, 384, 128, seed=11, std=1.5, key_offset=True)
+    _, _, v = workloads.prefill_inputs(1, 4, 2, 384, 128, seed=111)
     o, lse = run(q, k, v, True, scale)
     assert_attn_close(o, lse, *ref(q, k, v, True, scale), what="scale %g" % scale)
 
