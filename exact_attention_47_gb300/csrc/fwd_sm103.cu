@@ -22,6 +22,10 @@
 // warpgroup computes exponentials the tensor core works on the other tile,
 // and the completion of S_X(j+1) also proves PV_X(j) has finished, which
 // makes O_X and the P_X columns safe to touch again.
+// One thread needs about as long to issue an MMA as the MMA takes to run,
+// so the issuer tests the barriers of its next group while the last MMAs of
+// the current group are being issued, and never re-tests a stage it already
+// knows is full: no barrier round trip sits between two groups.
 //
 // The stabiliser m of a row ("Softmax stabiliser") is only moved when the
 // tile maximum exceeds it by more than 2^8 (in the exp2 domain), so O and l
@@ -185,54 +189,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
-      auto issue_s = [&](int x, int j) -> bool {
-        const int st = j % L::kStages;
-        if (!mbar_wait(smem_addr(&bar->k_full[st]), (j / L::kStages) & 1, wc)) return false;
-        tc_fence_after();
+      constexpr int kSteps = D / 16;               // MMAs in an S group (K = d)
+      constexpr int kPSteps = kBN / 16;            // MMAs in a PV group (K = keys)
+      const uint32_t kF = smem_addr(&bar->k_full[0]);
+      const uint32_t vF = smem_addr(&bar->v_full[0]);
+      const uint32_t pF = smem_addr(&bar->p_full[0]);
+      auto kfull = [&](int jj) { return kF + 8u * (jj % L::kStages); };
+      auto vfull = [&](int jj) { return vF + 8u * (jj % L::kStages); };
+      auto ph = [&](int jj) { return static_cast<uint32_t>((jj / L::kStages) & 1); };
+      // A dependency that was probed ready is not waited on again.
+      auto ensure = [&](uint32_t b, uint32_t parity, uint32_t probed) -> bool {
+        return probed != 0u || mbar_wait(b, parity, wc);
+      };
+      // Next group's probes: issued before the last two MMAs of a group.
+      uint32_t rA = 0, rB = 0;
+      int probe_kind = 0, probe_j = 0;             // 1: PV (P, V)  2: S (K)
+      auto do_probes = [&]() {
+        if (probe_kind == 1) {
+          rA = mbar_probe(pF + 8u * static_cast<uint32_t>(probe_j >> 16), probe_j & 1);
+          rB = mbar_probe(vfull(probe_j & 0xffff), ph(probe_j & 0xffff));
+        } else if (probe_kind == 2) {
+          rA = mbar_probe(kfull(probe_j), ph(probe_j));
+        }
+      };
+      auto group_s = [&](int x, int jj) {
+        const int st = jj % L::kStages;
         const uint32_t qbase = sQ + x * L::kQTile;
         const uint32_t kbase = sK + st * L::kKV;
         const uint32_t dS = tmem + (x ? L::kColS1 : L::kColS0);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < kSteps; ++kk) {
+          if (kk == kSteps - 2) do_probes();
           const uint64_t ad = sdesc_sw128(qbase + (kk >> 2) * L::kQChunk + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kKVChunk + (kk & 3) * 32, 16, 1024);
           umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(smem_addr(&bar->s_full[x]));
-        return true;
       };
-      auto issue_pv = [&](int x, int j) -> bool {
-        const int st = j % L::kStages;
-        if (!mbar_wait(smem_addr(&bar->p_full[x]), j & 1, wc)) return false;
-        if (!mbar_wait(smem_addr(&bar->v_full[st]), (j / L::kStages) & 1, wc)) return false;
-        tc_fence_after();
+      auto group_pv = [&](int x, int jj) {
+        const int st = jj % L::kStages;
         const uint32_t vbase = sV + st * L::kKV;
         const uint32_t aP = tmem + (x ? L::kColS1 : L::kColS0);
         const uint32_t dO = tmem + (x ? L::kColO1 : L::kColO0);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
+        for (int kk = 0; kk < kPSteps; ++kk) {
+          if (kk == kPSteps - 2) do_probes();
           // A = P from TMEM (8 columns = 16 keys per step), B = V (MN-major).
           const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kKVChunk, 1024);
-          umma_ts(dO, aP + kk * 8, bd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(dO, aP + kk * 8, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
-        return true;
       };
-      bool ok = mbar_wait(smem_addr(&bar->q_full), 0, wc);
-      if (ok) ok = issue_s(0, 0);
-      if (ok) ok = issue_s(1, 0);
-      if (ok) umma_commit(smem_addr(&bar->k_empty[0]));
+      // Schedule (each group probes what the next one needs):
+      //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+      bool ok = mbar_wait(smem_addr(&bar->q_full), 0, wc) && mbar_wait(kfull(0), 0, wc);
+      if (ok) {
+        tc_fence_after();
+        probe_kind = 0;
+        group_s(0, 0);
+        probe_kind = 1;                            // PV_A(0): P_A(0), V_0
+        probe_j = 0;
+        group_s(1, 0);
+        umma_commit(smem_addr(&bar->k_empty[0]));
+      }
       for (int j = 0; j < nB && ok; ++j) {
         const int st = j % L::kStages;
         if (j < nA) {
-          if (!(ok = issue_pv(0, j))) break;
+          // PV_A(j)
+          if (!(ok = ensure(pF, j & 1, rA) && ensure(vfull(j), ph(j), rB))) break;
+          tc_fence_after();
+          probe_kind = (j + 1 < nA) ? 2 : 0;       // S_A(j+1): K_{j+1}
+          probe_j = j + 1;
+          group_pv(0, j);
           if (j == nA - 1) umma_commit(smem_addr(&bar->o_done[0]));
+          if (j + 1 < nA) {
+            // S_A(j+1)
+            if (!(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+            tc_fence_after();
+            probe_kind = 1;                        // PV_B(j): P_B(j), V_j (known)
+            probe_j = (1 << 16) | j;
+            group_s(0, j + 1);
+            rB = 1;
+          } else {
+            rA = mbar_probe(pF + 8u, j & 1);
+            rB = 1;
+          }
+        } else {
+          rA = mbar_probe(pF + 8u, j & 1);
+          rB = mbar_probe(vfull(j), ph(j));
         }
-        if (j + 1 < nA && !(ok = issue_s(0, j + 1))) break;
-        if (!(ok = issue_pv(1, j))) break;
+        // PV_B(j)
+        if (!(ok = ensure(pF + 8u, j & 1, rA) && ensure(vfull(j), ph(j), rB))) break;
+        tc_fence_after();
+        probe_kind = (j + 1 < nB && j + 1 >= nA) ? 2 : 0;   // S_B(j+1) needs K_{j+1} if S_A did not test it
+        probe_j = j + 1;
+        group_pv(1, j);
         umma_commit(smem_addr(&bar->v_empty[st]));
         if (j == nB - 1) umma_commit(smem_addr(&bar->o_done[1]));
         if (j + 1 < nB) {
-          if (!(ok = issue_s(1, j + 1))) break;
+          // S_B(j+1)
+          if (j + 1 >= nA && !(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+          tc_fence_after();
+          probe_kind = (j + 1 < nA) ? 1 : 0;       // PV_A(j+1): P_A(j+1), V_{j+1}
+          probe_j = j + 1;
+          group_s(1, j + 1);
           umma_commit(smem_addr(&bar->k_empty[(j + 1) % L::kStages]));
         }
       }
@@ -298,9 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[c] = masked ? -INFINITY : s[c];
         }
       }
-      float mx = s[0];
+      // Row maximum: a depth-5 tree of three-input maxima.
+      float mx;
+      {
+        float t[43], u[15];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 42; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
+        t[42] = fmaxf(s[126], s[127]);
+#pragma unroll
+        for (int i = 0; i < 14; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+        u[14] = t[42];
+        mx = fmaxf(fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmax3(u[6], u[7], u[8])),
+                   fmax3(fmax3(u[9], u[10], u[11]), u[12], fmaxf(u[13], u[14])));
+      }
       const float mt = mx * sl2;
       if (j == 0) {
         m = (mt == -INFINITY) ? 0.f : mt;
@@ -313,50 +382,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           lr *= alpha;
           m = m_new;
           // O_X holds PV_X(0..j-1), complete since S_X(j) completed after it.
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             ATTN47_TMEM_LD32(tl + colO + c0, o);
             ATTN47_TMEM_LD_WAIT(o);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            for (int c = 0; c < 16; ++c) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1])), a2),
+                        lo, hi);
+              o[2 * c] = __float_as_uint(lo);
+              o[2 * c + 1] = __float_as_uint(hi);
+            }
             ATTN47_TMEM_ST32(tl + colO + c0, o);
           }
         }
       }
-      // Two denominators: `lr` sums the bf16-rounded numerators that P V
-      // uses, so O / lr weights every value row by exactly the factor it got;
-      // `l` sums the fp32 numerators and gives the LSE.
-      const float nm = -m;
-      float rs0 = 0.f, rs1 = 0.f, re0 = 0.f, re1 = 0.f;
-      uint32_t pk0[32], pk1[32];
+      // Numerators p = 2^(s * scale * log2 e - m), two lanes per instruction
+      // for the scale and the sums.  Two denominators: `lr` sums the
+      // bf16-rounded numerators that P V uses, so O / lr weights every value
+      // row by exactly the factor it got; `l` sums the fp32 numerators and
+      // gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
+      // 2c+1 in column c), the first half while the second is computed.
+      const uint64_t sc2 = f2_pack(sl2, sl2);
+      const uint64_t nm2 = f2_pack(-m, -m);
+      uint64_t accE[4] = {0, 0, 0, 0}, accR[4] = {0, 0, 0, 0};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(s[2 * c], sl2, nm));
-        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, nm));
-        const uint32_t w = pack_bf16x2(p0, p1);
-        re0 += p0;
-        re1 += p1;
-        rs0 += __uint_as_float(w << 16);
-        rs1 += __uint_as_float(w & 0xffff0000u);
-        pk0[c] = w;
-      }
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(s[64 + 2 * c], sl2, nm));
-        const float p1 = ex2(fmaf(s[64 + 2 * c + 1], sl2, nm));
-        const uint32_t w = pack_bf16x2(p0, p1);
-        re0 += p0;
-        re1 += p1;
-        rs0 += __uint_as_float(w << 16);
-        rs1 += __uint_as_float(w & 0xffff0000u);
-        pk1[c] = w;
+        for (int c = 0; c < 32; ++c) {
+          const int e = half * 64 + 2 * c;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), sc2, nm2), x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          const uint32_t w = pack_bf16x2(p0, p1);
+          accE[c & 3] = f2_add(accE[c & 3], f2_pack(p0, p1));
+          accR[c & 3] = f2_add(accR[c & 3],
+                               f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+          pk[c] = w;
+        }
+        ATTN47_TMEM_ST32(tl + colS + half * 32, pk);
       }
-      lr += rs0 + rs1;
-      l += re0 + re1;
-      // P_X over the first 64 columns of S_X (keys 2c, 2c+1 in column c).
-      ATTN47_TMEM_ST32(tl + colS + 0, pk0);
-      ATTN47_TMEM_ST32(tl + colS + 32, pk1);
+      {
+        float e0, e1, r0f, r1f;
+        f2_unpack(f2_add(f2_add(accE[0], accE[1]), f2_add(accE[2], accE[3])), e0, e1);
+        f2_unpack(f2_add(f2_add(accR[0], accR[1]), f2_add(accR[2], accR[3])), r0f, r1f);
+        l += e0 + e1;
+        lr += r0f + r1f;
+      }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -364,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
+    ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(smem_addr(&bar->o_done[x]), 0, wc)) {
       tc_fence_after();
       const float inv_l = 1.f / lr;
