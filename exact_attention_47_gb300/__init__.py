@@ -20,7 +20,7 @@ from ._binding import (  # noqa: F401
     library_path,
     load_library,
     selftest_wait_timeout,
-    set_decode_split_blocks,
+    set_decode_max_ctas,
     set_wait_timeout_ns,
     status_string,
 )

@@ -31,7 +31,7 @@ _SIGS = {
                                _P, _P, _P, ctypes.c_size_t, _P]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
-    "attn_set_decode_split_blocks": (None, [_I]),
+    "attn_set_decode_max_ctas": (None, [_I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_error": (ctypes.c_char_p, []),
@@ -194,8 +194,9 @@ def set_wait_timeout_ns(ns):
     load_library().attn_set_wait_timeout_ns(int(ns))
 
 
-def set_decode_split_blocks(blocks):
-    load_library().attn_set_decode_split_blocks(int(blocks))
+def set_decode_max_ctas(ctas):
+    """Cap the CTAs of a decode launch (0: one full wave)."""
+    load_library().attn_set_decode_max_ctas(int(ctas))
 
 
 def selftest_wait_timeout(timeout_ns, stream=None):

@@ -31,7 +31,7 @@ attn_status_t fail(attn_status_t s, const char* fmt, ...) {
 }
 
 unsigned long long g_timeout_ns = 1000000000ull;
-int g_decode_split_blocks = 0;  // 0 = choose per call
+int g_decode_max_ctas = 0;  // 0 = one full wave
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -119,17 +119,6 @@ attn_status_t launch_result(cudaError_t e, const char* what) {
   return ATTN_OK;
 }
 
-int decode_split_blocks(int num_seqs, int Hkv, int max_blocks, int sms) {
-  if (g_decode_split_blocks > 0) return g_decode_split_blocks;
-  // Largest split that still gives >= 8 CTAs per SM in the worst case.
-  for (int sb = attn47::kMaxSplitBlocks; sb > attn47::kMinSplitBlocks; sb /= 2) {
-    const long long units =
-        static_cast<long long>(num_seqs) * Hkv * ((max_blocks + sb - 1) / sb);
-    if (units >= 8LL * sms) return sb;
-  }
-  return attn47::kMinSplitBlocks;
-}
-
 __global__ void selftest_wait_kernel(unsigned int* status, unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
   __shared__ int abort_flag;
@@ -166,14 +155,7 @@ const char* attn_status_string(attn_status_t s) {
 
 void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns < 1000ull ? 1000ull : ns; }
 
-void attn_set_decode_split_blocks(int blocks) {
-  if (blocks <= 0) {
-    g_decode_split_blocks = 0;
-    return;
-  }
-  int b = blocks < attn47::kMinSplitBlocks ? attn47::kMinSplitBlocks : blocks;
-  g_decode_split_blocks = b > attn47::kMaxSplitBlocks ? attn47::kMaxSplitBlocks : b;
-}
+void attn_set_decode_max_ctas(int ctas) { g_decode_max_ctas = ctas > 0 ? ctas : 0; }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {
@@ -230,8 +212,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq) {
   if (num_seqs <= 0 || Hq <= 0 || d <= 0 || max_blocks_per_seq <= 0) return 0;
-  const int max_splits = (max_blocks_per_seq + attn47::kMinSplitBlocks - 1) / attn47::kMinSplitBlocks;
-  return attn47::decode_workspace_floats(num_seqs, Hq, d, max_splits) * sizeof(float);
+  return attn47::decode_workspace_bytes(num_seqs, Hq, d, max_blocks_per_seq);
 }
 
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -291,8 +272,8 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   a.d = d;
   a.max_blocks = max_blocks_per_seq;
   a.num_blocks = num_blocks;
-  a.split_blocks = decode_split_blocks(num_seqs, Hkv, max_blocks_per_seq, dev->sms);
-  a.max_splits = (max_blocks_per_seq + a.split_blocks - 1) / a.split_blocks;
+  a.sms = dev->sms;
+  a.max_ctas = g_decode_max_ctas;
   a.scale = scale;
   a.status = dev->status;
   a.timeout_ns = g_timeout_ns;

@@ -7,8 +7,9 @@
 
 namespace attn47 {
 
-constexpr int kMaxSplitBlocks = 32;   // logical blocks per split, upper bound
-constexpr int kMinSplitBlocks = 8;    // lower bound; sizes the workspace
+// Every decode CTA takes at least 2 * kMinSplitBlocks (sequence, KV head,
+// block) triples; this bounds the number of partial results per sequence.
+constexpr int kMinSplitBlocks = 8;
 
 struct DecLaunch {
   const CUtensorMap* tk;   // [num_blocks*Hkv*16, d] bf16, box {64, 16}, 128-byte swizzle
@@ -18,15 +19,18 @@ struct DecLaunch {
   const int* seq_lens;     // [num_seqs]
   void* o;                 // [num_seqs, Hq, d] bf16
   float* lse;              // [num_seqs, Hq] or nullptr
-  float* workspace;        // decode_workspace_floats(num_seqs, Hq, d, max_splits) floats
-  int num_seqs, Hq, Hkv, d, max_blocks, num_blocks, split_blocks, max_splits;
+  float* workspace;        // decode_workspace_bytes(...) bytes
+  int num_seqs, Hq, Hkv, d, max_blocks, num_blocks;
+  int sms;                 // SM count of the device
+  int max_ctas;            // 0: one full wave of CTAs
   float scale;
   unsigned int* status;
   unsigned long long timeout_ns;
   cudaStream_t stream;
 };
 
-size_t decode_workspace_floats(int num_seqs, int Hq, int d, int max_splits);
+int decode_max_parts(int max_blocks_per_seq);
+size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq);
 cudaError_t launch_decode_sm103(const DecLaunch& a);
 
 }  // namespace attn47

@@ -96,8 +96,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 /*
  * attn_decode_paged_workspace_size — bytes of device workspace that
- * attn_decode_paged needs for these sizes (fp32 partial results of the
- * key-range splits).  0 for an empty problem.
+ * attn_decode_paged needs for these sizes (fp32 partial results of
+ * sequences whose keys are split across CTAs, and a count per sequence).
+ * 0 for an empty problem.
  */
 size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq);
 
@@ -122,7 +123,9 @@ size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blo
  *  block_size must be 16; d must be 64 or 128; Hq % Hkv == 0 and
  *  Hq / Hkv <= 16; num_blocks * Hkv * 16 < 2^31.
  *  num_seqs == 0 is an empty problem: returns ATTN_OK, launches nothing.
- *  Launches two kernels (split decode, then merge).  Deterministic.
+ *  Launches two kernels (decode over an even split of all cached tokens,
+ *  then the merge of sequences split across CTAs).  Deterministic for a
+ *  given device and attn_set_decode_max_ctas setting.
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
@@ -146,13 +149,13 @@ attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out);
 void attn_set_wait_timeout_ns(unsigned long long ns);
 
 /*
- * attn_set_decode_split_blocks — number of logical blocks (8..32) that one
- * decode work unit covers; 0 (the default) lets each call choose from the
- * problem size and the SM count.  Values are clamped to [8, 32].  Any choice
- * gives the same result up to fp32 rounding order; it only changes how the
- * keys are spread over the SMs.  Applies to later calls from this process.
+ * attn_set_decode_max_ctas — upper bound on the CTAs of one decode launch;
+ * 0 (the default) launches one full wave (every SM, as many CTAs as fit).
+ * The cached tokens are split evenly over the CTAs; any setting gives the
+ * same result up to fp32 rounding order.  Applies to later calls from this
+ * process.
  */
-void attn_set_decode_split_blocks(int blocks);
+void attn_set_decode_max_ctas(int ctas);
 
 /*
  * attn_selftest_wait_timeout — launches a one-warp kernel that waits on a

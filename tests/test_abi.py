@@ -90,8 +90,9 @@ def test_decode_host_validation(lib):
 
 
 def test_workspace_size_formula(lib):
-    # fp32 partial O (d floats) + max and sum per (seq, head, split of >= 8 blocks)
-    assert lib.attn_decode_paged_workspace_size(64, 12, 128, 256) == 64 * 12 * 32 * 130 * 4
+    # fp32 partial O (d floats) + max and sum per (seq, head, part) with at
+    # most ceil(256 / 16) + 1 parts, plus one int count per (seq, head)
+    assert lib.attn_decode_paged_workspace_size(64, 12, 128, 256) == 64 * 12 * 17 * 130 * 4 + 64 * 12 * 4
     assert lib.attn_decode_paged_workspace_size(0, 12, 128, 256) == 0
 
 

@@ -107,15 +107,19 @@ def test_decode_equals_prefill_last_row():
     assert (l_fwd[0, :, L - 1] - l_dec[0]).abs().max().item() <= 1e-3
 
 
-@pytest.mark.parametrize("split", [8, 16, 32])
-def test_split_size_does_not_change_the_result(split):
-    inp = workloads.decode_inputs(5, 12, 2, 128, seed=25, len_lo=1, len_hi=2000)
+@pytest.mark.parametrize("ctas", [1, 3, 7, 64, 0])
+def test_work_split_does_not_change_the_result(ctas):
+    """One CTA walks every sequence; a few CTAs split sequences into many
+    parts; a full wave gives the minimum chunk.  All agree with the oracle."""
+    inp = workloads.decode_inputs(9, 12, 2, 128, seed=25, len_lo=1, len_hi=2000,
+                                  seq_lens=[1, 700, 0, 17, 2000, 256, 1999, 33, 1024])
     try:
-        attn.set_decode_split_blocks(split)
+        attn.set_decode_max_ctas(ctas)
         o, lse = run(inp, 0.1)
     finally:
-        attn.set_decode_split_blocks(0)
-    assert_attn_close(o, lse, *ref(inp, 0.1), what="split %d" % split)
+        attn.set_decode_max_ctas(0)
+    assert attn.device_status() == 0
+    assert_attn_close(o, lse, *ref(inp, 0.1), what="ctas %d" % ctas)
 
 
 def test_deterministic():
