@@ -261,6 +261,8 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   a.tk = &tk;
   a.tv = &tv;
   a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.o = o;

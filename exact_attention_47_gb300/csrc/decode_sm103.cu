@@ -14,10 +14,11 @@
 // whatever the length mix.  The chunk is walked as segments (maximal runs of
 // one (b, g)); the G = Hq/Hkv query heads sharing KV head g are processed
 // together so each K/V block is read from HBM once.
-//   warp 4      producer: plans the chunk from seq_lens, then per segment
-//               bulk-copies the G query rows, and per block translates the
-//               table entry and TMA-copies the (block, head) K and V slices
-//               (16 x d bf16, 128-byte swizzle) into an 8-stage ring
+//   warp 4      producer: plans the chunk from seq_lens; translates table
+//               entries a batch of 32 blocks ahead; per segment bulk-copies
+//               the G query rows; per
+//               block TMA-copies the (block, head) K and V slices (16 x d
+//               bf16, 128-byte swizzle) into an 8-stage ring
 //   warps 0..3  consumers: block c of the chunk goes to warp c % 4; scores
 //               and P V are 16x8x16 warp MMAs (rows = the G query heads,
 //               zero-padded to 16); at the segment's end the four warp states
@@ -73,6 +74,8 @@ static_assert(kStages % kConsumers == 0, "a stage must map to one consumer warp"
 
 struct DecParams {
   const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
   const int* block_table;
   const int* seq_lens;
   __nv_bfloat16* o;
@@ -108,6 +111,21 @@ struct SegWalk {
   }
   // Current segment: blocks [blk, blk + count()) of (b, g).
   __device__ int count() const { return min(remaining, nblk - blk); }
+  // Move k blocks forward (possibly across segments).
+  __device__ void skip(const DecParams& p, int k) {
+    while (k > 0 && remaining > 0) {
+      const int c = count();
+      if (k < c) {
+        blk += k;
+        remaining -= k;
+        flat += k;
+        k = 0;
+      } else {
+        advance(p, c);
+        k -= c;
+      }
+    }
+  }
   __device__ void advance(const DecParams& p, int cnt) {
     remaining -= cnt;
     flat += cnt;
@@ -146,17 +164,20 @@ __global__ void __launch_bounds__(kThreads)
   if (warp == kConsumers) {
     int T = 0;
     bool bad = false;
-    for (int base = 0; base < p.num_seqs; base += 32) {
-      const int b = base + lane;
-      int nb = 0;
-      if (b < p.num_seqs) {
-        const int L = p.seq_lens[b];
-        bad |= (L < 0 || L > p.max_blocks * kBS);
-        nb = seq_blocks(p, b) * p.Hkv;
-      }
+    for (int base = 0; base < p.num_seqs; base += 128) {
+      int nb[4];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, o);
-      T += nb;
+      for (int u = 0; u < 4; ++u) {              // four independent loads in flight
+        const int b = base + 32 * u + lane;
+        const int L = b < p.num_seqs ? p.seq_lens[b] : 0;
+        bad |= (L < 0 || L > p.max_blocks * kBS);
+        const int Lc = L < 0 ? 0 : min(L, p.max_blocks * kBS);
+        nb[u] = (Lc + kBS - 1) / kBS * p.Hkv;
+      }
+      int sum = (nb[0] + nb[1]) + (nb[2] + nb[3]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      T += sum;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0)
       atomicOr(p.status, kDevBadSeqLen);
@@ -216,63 +237,86 @@ __global__ void __launch_bounds__(kThreads)
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    SegWalk w;
-    w.start(p, b0, off0, c0, c1);
-    int issued = 0, seg = 0;
-    bool ok = true;
-    const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
-    while (ok && w.remaining > 0) {
-      const int cnt = w.count();
-      // The segment's query rows.
-      const int qs = seg % kQSlots;
-      if (lane == 0) {
-        ok = mbar_wait(smem_addr(&sh->qempty[qs]), ((seg / kQSlots) & 1) ^ 1, wc);
-        if (ok) {
-          const uint32_t qb = smem_addr(&sh->qfull[qs]);
-          mbar_arrive_expect_tx(qb, qbytes);
-          bulk_load(qring + qs * Lt::kQSlot,
-                    p.q + (static_cast<size_t>(w.b) * p.Hq + w.g * G) * D, qbytes, qb);
+    // Lane j handles chunk blocks j, 32 + j, 64 + j, ...: it translates the
+    // table entry up to a batch of 32 blocks before the block is copied, so
+    // no table lookup sits between two copies.
+    const int nblocks = c1 - c0;
+    SegWalk lw;
+    lw.start(p, b0, off0, c0, c1);
+    lw.skip(p, lane);
+    auto fetch = [&](int k, int& ph, int& bb, int& gg) {
+      ph = -1;
+      bb = -1;
+      gg = 0;
+      if (k < nblocks && lw.remaining > 0) {
+        bb = lw.b;
+        gg = lw.g;
+        ph = p.block_table[static_cast<size_t>(lw.b) * p.max_blocks + lw.blk];
+        if (ph < 0 || ph >= p.num_blocks) {
+          atomicOr(p.status, kDevBadBlock);
+          ph = -1;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      ++seg;
-      const int* row = p.block_table + static_cast<size_t>(w.b) * p.max_blocks + w.blk;
-      for (int i0 = 0; i0 < cnt && ok; i0 += 32) {
-        // 32 table entries translated at once, issued one by one.
-        int ph = (i0 + lane < cnt) ? row[i0 + lane] : 0;
-        const bool badb = (i0 + lane < cnt) && (ph < 0 || ph >= p.num_blocks);
-        if (badb) ph = -1;
-        if (__any_sync(0xffffffffu, badb) && lane == 0) atomicOr(p.status, kDevBadBlock);
-        const int n = min(32, cnt - i0);
-        for (int i = 0; i < n; ++i) {
-          const int phys = __shfl_sync(0xffffffffu, ph, i);
-          if (lane == 0) {
-            const int st = issued % kStages;
-            ok = mbar_wait(smem_addr(&sh->empty[st]), ((issued / kStages) & 1) ^ 1, wc);
-            if (ok) {
-              const uint32_t fb = smem_addr(&sh->full[st]);
-              sh->phys[st] = phys;
-              if (phys >= 0) {
-                const int rowk = (phys * p.Hkv + w.g) * kBS;
-                const uint32_t dst = ring + st * Lt::kStage;
-                mbar_arrive_expect_tx(fb, Lt::kStage);
-#pragma unroll
-                for (int c = 0; c < Lt::kChunks; ++c) {
-                  tma_load_2d(dst + c * Lt::kBox, &tk, fb, c * 64, rowk);
-                  tma_load_2d(dst + Lt::kHalf + c * Lt::kBox, &tv, fb, c * 64, rowk);
-                }
-              } else {
-                mbar_arrive(fb);
-              }
-            }
+    };
+    int cur_ph, cur_b, cur_g, nxt_ph, nxt_b, nxt_g;
+    fetch(lane, cur_ph, cur_b, cur_g);
+    lw.skip(p, 32);
+    fetch(32 + lane, nxt_ph, nxt_b, nxt_g);
+
+    int issued = 0, seg = 0, pb = -1, pg = -1;
+    bool ok = true;
+    const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
+    for (int c = 0; c < nblocks && ok; ++c) {
+      const int j = c & 31;
+      if (j == 0 && c > 0) {
+        cur_ph = nxt_ph;
+        cur_b = nxt_b;
+        cur_g = nxt_g;
+        lw.skip(p, 32);
+        fetch(c + 32 + lane, nxt_ph, nxt_b, nxt_g);
+      }
+      const int phys = __shfl_sync(0xffffffffu, cur_ph, j);
+      const int b = __shfl_sync(0xffffffffu, cur_b, j);
+      const int g = __shfl_sync(0xffffffffu, cur_g, j);
+      if (lane == 0) {
+        if (b != pb || g != pg) {
+          // First block of a segment: its query rows.
+          const int qs = seg % kQSlots;
+          ok = mbar_wait(smem_addr(&sh->qempty[qs]), ((seg / kQSlots) & 1) ^ 1, wc);
+          if (ok) {
+            const uint32_t qb = smem_addr(&sh->qfull[qs]);
+            mbar_arrive_expect_tx(qb, qbytes);
+            bulk_load(qring + qs * Lt::kQSlot, p.q + (static_cast<size_t>(b) * p.Hq + g * G) * D,
+                      qbytes, qb);
           }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
+          ++seg;
+          pb = b;
+          pg = g;
+        }
+        const int st = issued % kStages;
+        if (ok) ok = mbar_wait(smem_addr(&sh->empty[st]), ((issued / kStages) & 1) ^ 1, wc);
+        if (ok) {
+          const uint32_t fb = smem_addr(&sh->full[st]);
+          sh->phys[st] = phys;
+          if (phys >= 0) {
+            const int rowk = (phys * p.Hkv + g) * kBS;
+            const uint32_t dst = ring + st * Lt::kStage;
+            mbar_arrive_expect_tx(fb, Lt::kStage);
+#pragma unroll
+            for (int cc = 0; cc < Lt::kChunks; ++cc) {
+              tma_load_2d(dst + cc * Lt::kBox, &tk, fb, cc * 64, rowk);
+              tma_load_2d(dst + Lt::kHalf + cc * Lt::kBox, &tv, fb, cc * 64, rowk);
+            }
+          } else {
+            mbar_arrive(fb);
+          }
           ++issued;
         }
       }
-      w.advance(p, cnt);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    seg = __shfl_sync(0xffffffffu, seg, 0);
     // Every copy issued must have landed before the CTA may exit.
     if (lane == 0) {
       for (int st = 0; st < kStages && st < issued; ++st) {
@@ -580,6 +624,8 @@ cudaError_t launch_t(const DecLaunch& a) {
   int* nparts = reinterpret_cast<int*>(ws_ml + static_cast<size_t>(a.num_seqs) * a.Hq * max_parts * 2);
   DecParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  p.k_cache = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
+  p.v_cache = reinterpret_cast<const __nv_bfloat16*>(a.v_cache);
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.o = reinterpret_cast<__nv_bfloat16*>(a.o);

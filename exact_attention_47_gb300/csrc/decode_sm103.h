@@ -15,6 +15,8 @@ struct DecLaunch {
   const CUtensorMap* tk;   // [num_blocks*Hkv*16, d] bf16, box {64, 16}, 128-byte swizzle
   const CUtensorMap* tv;
   const void* q;           // [num_seqs, Hq, d] bf16
+  const void* k_cache;     // [num_blocks, Hkv, 16, d] bf16
+  const void* v_cache;
   const int* block_table;  // [num_seqs, max_blocks]
   const int* seq_lens;     // [num_seqs]
   void* o;                 // [num_seqs, Hq, d] bf16

@@ -210,6 +210,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Contiguous global -> L2 prefetch (no destination; 16-byte aligned, size a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
 // Programmatic dependent launch: let the next kernel in the stream start /
 // wait until the previous kernel's results are visible.
 __device__ __forceinline__ void pdl_launch_dependents() {
