@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     AttnError,
     abi_version,
     attn_decode_paged,
+    attn_decode_paged_noalloc,
     attn_decode_paged_workspace_size,
     attn_fwd,
     device_status,

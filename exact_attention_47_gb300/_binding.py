@@ -29,6 +29,8 @@ _SIGS = {
     "attn_decode_paged_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, ctypes.c_size_t, _P]),
+    "attn_decode_paged_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                                       _P, _P, _P]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
@@ -179,6 +181,40 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, o=
                                float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check("attn_decode_paged", st)
+    return o, lse
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=None, o=None,
+                              lse=None, return_lse=True, stream=None):
+    """attn_decode_paged without a workspace argument, for callers that may
+    not allocate device memory when they run the decode: the library uses
+    its own fixed 8 MiB device array instead (sizes needing more raise
+    AttnError with ATTN_ERR_WORKSPACE).  Calls that overlap on the GPU share
+    that array and must be ordered.  Only the outputs, if not given, are
+    allocated here, by torch; pass ``o`` (and ``lse`` or return_lse=False)
+    to allocate nothing at all."""
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
+                        ("v_cache", v_cache, torch.bfloat16), ("block_table", block_table, torch.int32),
+                        ("seq_lens", seq_lens, torch.int32)):
+        _need_cuda(name, t, dt)
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [S,Hq,d] and caches [num_blocks,Hkv,block_size,d]")
+    S, Hq, d = q.shape
+    num_blocks, Hkv, block_size, _ = k_cache.shape
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need_cuda("o", o, torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
+    st = lib.attn_decode_paged_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                       _ptr(seq_lens), S, Hq, Hkv, d, block_size,
+                                       block_table.shape[1], num_blocks, float(scale), _ptr(o),
+                                       _ptr(lse), _stream_handle(stream))
+    _check("attn_decode_paged_noalloc", st)
     return o, lse
 
 

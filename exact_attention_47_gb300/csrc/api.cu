@@ -18,6 +18,13 @@
 // Per-device error word written by the kernels (ATTN_DEV_* bits).
 __device__ unsigned int g_attn47_status;
 
+// Fixed scratch of attn_decode_paged_noalloc: the partial results of
+// sequences whose keys are split across CTAs.  Every device that loads the
+// library holds it until the process exits; every call of that entry point
+// on a device reuses it.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB
+static __device__ __align__(256) unsigned char g_attn47_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 thread_local char g_last_error[512] = "";
@@ -39,6 +46,7 @@ struct DeviceInfo {
   bool usable = false;
   int sms = 0;
   unsigned int* status = nullptr;
+  void* noalloc_scratch = nullptr;   // device address of the fixed scratch array
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -281,6 +289,43 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
   a.timeout_ns = g_timeout_ns;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_result(attn47::launch_decode_sm103(a), "attn_decode_paged");
+}
+
+attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int num_seqs, int Hq, int Hkv, int d, int block_size,
+                                        int max_blocks_per_seq, int num_blocks, float scale,
+                                        void* o, float* lse, void* stream) {
+  const size_t need = attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq);
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_WORKSPACE,
+                "this decode needs %zu bytes of scratch but the built-in array of "
+                "attn_decode_paged_noalloc holds %zu; call attn_decode_paged with a workspace",
+                need, kNoAllocScratchBytes);
+  if (num_seqs <= 0 || need == 0)   // empty or invalid sizes: same answer as attn_decode_paged
+    return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
+                             block_size, max_blocks_per_seq, num_blocks, scale, o, lse, nullptr,
+                             0, stream);
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  void* scratch = nullptr;
+  {
+    // One-time set-up per device (this device is current): the host-side
+    // name of the array is not a device address, so look the address up.
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (dev->noalloc_scratch == nullptr) {
+      void* addr = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&addr, g_attn47_noalloc_scratch);
+      if (e != cudaSuccess || addr == nullptr)
+        return fail(ATTN_ERR_DEVICE, "scratch array address unavailable: %s", cudaGetErrorString(e));
+      dev->noalloc_scratch = addr;
+    }
+    scratch = dev->noalloc_scratch;
+  }
+  return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
+                           block_size, max_blocks_per_seq, num_blocks, scale, o, lse, scratch,
+                           kNoAllocScratchBytes, stream);
 }
 
 attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {

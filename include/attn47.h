@@ -134,6 +134,38 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_paged_noalloc — attn_decode_paged without a caller-provided
+ * workspace.  (The pages describe no such call: it exists only for callers
+ * of this library that cannot allocate device memory at the time they run
+ * the decode — for example a plugin inside a host framework that owns all
+ * device memory and forbids its extensions from calling cudaMalloc, or a
+ * latency-bound serving loop that must not call cudaMalloc/cudaFree because
+ * they can synchronize the whole device.)
+ *
+ *  Arguments, layouts, results and errors are those of attn_decode_paged,
+ *  minus workspace and workspace_bytes.  Instead the library uses one fixed
+ *  8 MiB array of device memory that it declares itself; it is part of the
+ *  library image, so every device that loads the library holds it until the
+ *  process exits.  No device memory is allocated by the call: it makes no
+ *  cudaMalloc, cudaFree or other allocating call.
+ *  - Limit: if attn_decode_paged_workspace_size(num_seqs, Hq, d,
+ *    max_blocks_per_seq) exceeds 8 MiB the call returns ATTN_ERR_WORKSPACE
+ *    and launches nothing (use attn_decode_paged for such sizes).
+ *  - The first call on each device looks up the array's device address once
+ *    (with that device current); make that first call before any stream
+ *    capture begins.
+ *  - All calls on one device share the array and it keeps the previous
+ *    call's contents; nothing in it needs to start at zero.  Calls whose
+ *    kernels overlap on the GPU (different streams, no ordering between
+ *    them) race on the array and may produce wrong results: order them.
+ */
+attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int num_seqs, int Hq, int Hkv, int d, int block_size,
+                                        int max_blocks_per_seq, int num_blocks, float scale,
+                                        void* o, float* lse, void* stream);
+
+/*
  * attn_get_device_status — synchronises `stream`, copies the current
  * device's status word (ATTN_DEV_* bits) to *flags_out (host pointer) and
  * clears it.  Returns ATTN_ERR_DEVICE if the device is unusable.
