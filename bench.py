@@ -44,9 +44,10 @@ DEC_CFG = "paged_decode"
 NSETS = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
-# ncu summaries (profiles/); None until captured for the current kernels.
-TRAFFIC_FWD = None
-TRAFFIC_DEC = None
+# ncu summaries (profiles/), taken on this workload; None once a kernel changes
+# until it is captured again.  Decode: main kernel + merge kernel.
+TRAFFIC_FWD = 67185664 + 9444096
+TRAFFIC_DEC = (132289792 + 3985920) + (1409280 + 0)
 
 
 def peaks():
