@@ -220,6 +220,24 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- GPU arm
 
+def max_over_ranks(values, dist, device):
+    """Each rank's timings -> the slowest rank's, on every rank."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rates(world, steps, flops, dbytes, fwd_sum_ms, dec_sum_ms):
+    """Whole-job forward TFLOP/s and decode GB/s (every rank runs the same
+    work, timed by the slowest rank) and the per-GPU rates of one launch."""
+    fwd_avg_s = fwd_sum_ms / steps / 1e3
+    dec_avg_s = dec_sum_ms / steps / 1e3
+    achieved_fwd = flops / fwd_avg_s / 1e12
+    achieved_dec = dbytes / dec_avg_s / 1e9
+    return world * achieved_fwd, world * achieved_dec, achieved_fwd, achieved_dec
+
+
 def build_sets(rank, device):
     import exact_attention_47_gb300 as attn
 
@@ -347,21 +365,12 @@ def run_gpu(args, rank, world, local_rank):
     clock.stop()
 
     # ---- max over ranks
-    fwd_sum = sum(fwd_ms)
-    dec_sum = sum(dec_ms)
-    vals = torch.tensor([total_ms, fwd_sum, dec_sum, e2e_ms], dtype=torch.float64, device=device)
-    if dist:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    total_ms, fwd_sum, dec_sum, e2e_ms = vals.tolist()
+    total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
+        [total_ms, sum(fwd_ms), sum(dec_ms), e2e_ms], dist, device)
 
     if rank == 0:
         pk, pk_kind = peaks()
-        fwd_avg_s = fwd_sum / K / 1e3
-        dec_avg_s = dec_sum / K / 1e3
-        tflops = world * flops / fwd_avg_s / 1e12
-        gbs = world * dbytes / dec_avg_s / 1e9
-        achieved_fwd = flops / fwd_avg_s / 1e12
-        achieved_dec = dbytes / dec_avg_s / 1e9
+        tflops, gbs, achieved_fwd, achieved_dec = job_rates(world, K, flops, dbytes, fwd_sum, dec_sum)
         line = {
             "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
