@@ -22,9 +22,10 @@
 // warpgroup computes exponentials the tensor core works on the other tile,
 // and the completion of S_X(j+1) also proves PV_X(j) has finished, which
 // makes O_X and the P_X columns safe to touch again.
-// One thread needs about as long to issue an MMA as the MMA takes to run,
-// so the issuer tests the barriers of its next group while the last MMAs of
-// the current group are being issued, and never re-tests a stage it already
+// The whole MMA warp runs the issuing schedule and one elected lane issues,
+// so descriptors and barrier addresses stay warp-uniform values.  The
+// issuer tests the barriers of its next group while the last MMAs of the
+// current group are being issued, and never re-tests a stage it already
 // knows is full: no barrier round trip sits between two groups.
 //
 // The stabiliser m of a row ("Softmax stabiliser") is only moved when the
@@ -47,11 +48,11 @@ constexpr int kThreads = 384;       // 2 softmax warpgroups + 1 producer/MMA war
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 // Launched at 168 registers a thread (384 x 168 = 64512); the softmax
-// warpgroups then take 224 and the producer/MMA warpgroup keeps 56:
-// 256 x 224 + 128 x 56 = 64512, and per sub-partition 224 + 224 + 56 = 504
+// warpgroups then take 216 and the producer/MMA warpgroup keeps 72:
+// 256 x 216 + 128 x 72 = 64512, and per sub-partition 216 + 216 + 72 = 504
 // = 3 x 168, so the increase never waits for registers nobody frees.
-constexpr uint32_t kRegsSoftmax = 224;
-constexpr uint32_t kRegsOther = 56;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 72;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;        // lazy-rescale threshold, log2 units
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
       constexpr int kSteps = D / 16;               // MMAs in an S group (K = d)
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto ph = [&](int jj) { return static_cast<uint32_t>((jj / L::kStages) & 1); };
       // A dependency that was probed ready is not waited on again.
       auto ensure = [&](uint32_t b, uint32_t parity, uint32_t probed) -> bool {
-        return probed != 0u || mbar_wait(b, parity, wc);
+        return __all_sync(0xffffffffu, probed != 0u) || mbar_wait_warp(b, parity, wc);
       };
       // Next group's probes: issued before the last two MMAs of a group.
       uint32_t rA = 0, rB = 0;
@@ -222,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kk == kSteps - 2) do_probes();
           const uint64_t ad = sdesc_sw128(qbase + (kk >> 2) * L::kQChunk + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kKVChunk + (kk & 3) * 32, 16, 1024);
-          umma_ss(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+          umma_ss_warp(dS, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
         }
-        umma_commit(smem_addr(&bar->s_full[x]));
+        umma_commit_warp(smem_addr(&bar->s_full[x]));
       };
       auto group_pv = [&](int x, int jj) {
         const int st = jj % L::kStages;
@@ -236,12 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kk == kPSteps - 2) do_probes();
           // A = P from TMEM (8 columns = 16 keys per step), B = V (MN-major).
           const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kKVChunk, 1024);
-          umma_ts(dO, aP + kk * 8, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_ts_warp(dO, aP + kk * 8, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
       };
       // Schedule (each group probes what the next one needs):
       //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
-      bool ok = mbar_wait(smem_addr(&bar->q_full), 0, wc) && mbar_wait(kfull(0), 0, wc);
+      bool ok = mbar_wait_warp(smem_addr(&bar->q_full), 0, wc) && mbar_wait_warp(kfull(0), 0, wc);
       if (ok) {
         tc_fence_after();
         probe_kind = 0;
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         probe_kind = 1;                            // PV_A(0): P_A(0), V_0
         probe_j = 0;
         group_s(1, 0);
-        umma_commit(smem_addr(&bar->k_empty[0]));
+        umma_commit_warp(smem_addr(&bar->k_empty[0]));
       }
       for (int j = 0; j < nB && ok; ++j) {
         const int st = j % L::kStages;
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           probe_kind = (j + 1 < nA) ? 2 : 0;       // S_A(j+1): K_{j+1}
           probe_j = j + 1;
           group_pv(0, j);
-          if (j == nA - 1) umma_commit(smem_addr(&bar->o_done[0]));
+          if (j == nA - 1) umma_commit_warp(smem_addr(&bar->o_done[0]));
           if (j + 1 < nA) {
             // S_A(j+1)
             if (!(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
@@ -283,8 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         probe_kind = (j + 1 < nB && j + 1 >= nA) ? 2 : 0;   // S_B(j+1) needs K_{j+1} if S_A did not test it
         probe_j = j + 1;
         group_pv(1, j);
-        umma_commit(smem_addr(&bar->v_empty[st]));
-        if (j == nB - 1) umma_commit(smem_addr(&bar->o_done[1]));
+        umma_commit_warp(smem_addr(&bar->v_empty[st]));
+        if (j == nB - 1) umma_commit_warp(smem_addr(&bar->o_done[1]));
         if (j + 1 < nB) {
           // S_B(j+1)
           if (j + 1 >= nA && !(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
@@ -292,12 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           probe_kind = (j + 1 < nA) ? 1 : 0;       // PV_A(j+1): P_A(j+1), V_{j+1}
           probe_j = j + 1;
           group_s(1, j + 1);
-          umma_commit(smem_addr(&bar->k_empty[(j + 1) % L::kStages]));
+          umma_commit_warp(smem_addr(&bar->k_empty[(j + 1) % L::kStages]));
         }
       }
       // All issued MMAs must retire before TMEM is released.
-      umma_commit(smem_addr(&bar->mma_final));
-      mbar_wait(smem_addr(&bar->mma_final), 0, wc, true);
+      umma_commit_warp(smem_addr(&bar->mma_final));
+      __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
     }
   }
     // Each role ends on the same named barrier, so the register-split
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 2c+1 in column c), the first half while the second is computed.
       const uint64_t sc2 = f2_pack(sl2, sl2);
       const uint64_t nm2 = f2_pack(-m, -m);
-      uint64_t accE[4] = {0, 0, 0, 0}, accR[4] = {0, 0, 0, 0};
+      uint64_t accE[4] = {0, 0, 0, 0};
+      float accR[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -420,18 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = ex2(x0), p1 = ex2(x1);
           const uint32_t w = pack_bf16x2(p0, p1);
           accE[c & 3] = f2_add(accE[c & 3], f2_pack(p0, p1));
-          accR[c & 3] = f2_add(accR[c & 3],
-                               f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)));
+          accR[(c & 1) * 2] = add_bf16lo_f32(w, accR[(c & 1) * 2]);
+          accR[(c & 1) * 2 + 1] = add_bf16hi_f32(w, accR[(c & 1) * 2 + 1]);
           pk[c] = w;
         }
         ATTN47_TMEM_ST32(tl + colS + half * 32, pk);
       }
       {
-        float e0, e1, r0f, r1f;
+        float e0, e1;
         f2_unpack(f2_add(f2_add(accE[0], accE[1]), f2_add(accE[2], accE[3])), e0, e1);
-        f2_unpack(f2_add(f2_add(accR[0], accR[1]), f2_add(accR[2], accR[3])), r0f, r1f);
         l += e0 + e1;
-        lr += r0f + r1f;
+        lr += (accR[0] + accR[1]) + (accR[2] + accR[3]);
       }
       tmem_st_wait();
       tc_fence_before();
