@@ -43,6 +43,10 @@ constexpr int kThreads = (kConsumers + 1) * 32;
 constexpr int kStages = 8;
 constexpr int kQSlots = 2;
 constexpr int kMinChunk = 2 * kMinSplitBlocks;   // block-heads per CTA, lower bound
+// A CTA pays about this many blocks' worth of time to start a (sequence,
+// KV head) run (query load, state merge, output write), so work is split by
+// cost = blocks + kRunCost per run, not by blocks alone.
+constexpr int kRunCost = 3;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -67,6 +71,7 @@ struct DecShared {
   uint64_t qempty[kQSlots];
   int phys[kStages];
   int c0, c1, chunk, b0, off0;
+  int cost0;                    // first cost unit of this CTA (chunk is in cost units)
   int abort;
 };
 static_assert(sizeof(DecShared) <= 256, "shared control block");
@@ -159,61 +164,90 @@ __global__ void __launch_bounds__(kThreads)
   const int G = p.group;
 
   // ------------------------------------------------------------------ plan
-  // Total work T = sum_b Hkv * ceil(L_b / 16) block-heads; this CTA takes
-  // [c0, c1) with chunk = max(kMinChunk, ceil(T / grid)).
+  // Work: the block-heads of every (sequence, KV head) run, T in all; each
+  // run also costs kRunCost to start.  With C = T + kRunCost x (runs), this
+  // CTA takes the cost units [cost0, cost0 + chunk), chunk = max(kMinChunk,
+  // ceil(C / grid)), and with them the blocks [c0, c1) in flat order: the
+  // start cost of a run sits just before its block 0.
   if (warp == kConsumers) {
-    int T = 0;
+    int T = 0, C = 0;
     bool bad = false;
     for (int base = 0; base < p.num_seqs; base += 128) {
-      int nb[4];
+      int nb[4], nc[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {              // four independent loads in flight
         const int b = base + 32 * u + lane;
         const int L = b < p.num_seqs ? p.seq_lens[b] : 0;
         bad |= (L < 0 || L > p.max_blocks * kBS);
         const int Lc = L < 0 ? 0 : min(L, p.max_blocks * kBS);
-        nb[u] = (Lc + kBS - 1) / kBS * p.Hkv;
+        const int blocks = (Lc + kBS - 1) / kBS;
+        nb[u] = blocks * p.Hkv;
+        nc[u] = blocks > 0 ? (blocks + kRunCost) * p.Hkv : 0;
       }
       int sum = (nb[0] + nb[1]) + (nb[2] + nb[3]);
+      int csum = (nc[0] + nc[1]) + (nc[2] + nc[3]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      for (int o = 16; o > 0; o >>= 1) {
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        csum += __shfl_xor_sync(0xffffffffu, csum, o);
+      }
       T += sum;
+      C += csum;
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0)
       atomicOr(p.status, kDevBadSeqLen);
     const int grid = static_cast<int>(gridDim.x);
-    const int chunk = max(kMinChunk, (T + grid - 1) / grid);
-    const int c0 = static_cast<int>(blockIdx.x) * chunk;
-    const int c1 = min(T, c0 + chunk);
-    int b0 = -1, off0 = 0;
-    if (c0 < T) {
-      int P = 0;
-      for (int base = 0; base < p.num_seqs && b0 < 0; base += 32) {
+    const int chunk = max(kMinChunk, (C + grid - 1) / grid);
+    const int cost0 = static_cast<int>(blockIdx.x) * chunk;
+    const int cost1 = min(C, cost0 + chunk);
+    // Flat block position (and sequence, offset in it) of a cost position.
+    auto locate = [&](int cost, int& flat, int& bq, int& off) {
+      flat = T;
+      bq = -1;
+      off = 0;
+      if (cost >= C) return;
+      int P = 0, F = 0;
+      for (int base = 0; base < p.num_seqs && bq < 0; base += 32) {
         const int b = base + lane;
-        const int nb = (b < p.num_seqs) ? seq_blocks(p, b) * p.Hkv : 0;
-        int incl = nb;
+        const int blocks = (b < p.num_seqs) ? seq_blocks(p, b) : 0;
+        const int nc = blocks > 0 ? (blocks + kRunCost) * p.Hkv : 0;
+        int incl = nc, fincl = blocks * p.Hkv;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          const int fy = __shfl_up_sync(0xffffffffu, fincl, o);
+          if (lane >= o) {
+            incl += y;
+            fincl += fy;
+          }
         }
-        const int excl = incl - nb;
-        const bool here = nb > 0 && P + excl <= c0 && c0 < P + incl;
+        const int excl = incl - nc;
+        const bool here = nc > 0 && P + excl <= cost && cost < P + incl;
         const unsigned hit = __ballot_sync(0xffffffffu, here);
         if (hit) {
           const int src = __ffs(hit) - 1;
-          b0 = base + src;
-          off0 = c0 - P - __shfl_sync(0xffffffffu, excl, src);
+          bq = base + src;
+          const int nblk = __shfl_sync(0xffffffffu, blocks, src);
+          const int rel = cost - P - __shfl_sync(0xffffffffu, excl, src);
+          const int g = rel / (nblk + kRunCost);
+          const int blk = max(0, rel % (nblk + kRunCost) - kRunCost);
+          off = g * nblk + blk;
+          flat = F + __shfl_sync(0xffffffffu, fincl - blocks * p.Hkv, src) + off;
         }
         P += __shfl_sync(0xffffffffu, incl, 31);
+        F += __shfl_sync(0xffffffffu, fincl, 31);
       }
-    }
+    };
+    int c0, b0, off0, c1, b1, off1;
+    locate(cost0, c0, b0, off0);
+    locate(cost1, c1, b1, off1);
     if (lane == 0) {
       sh->c0 = c0;
       sh->c1 = c1;
       sh->chunk = chunk;
-      sh->b0 = b0;
+      sh->b0 = (c0 < c1) ? b0 : -1;
       sh->off0 = off0;
+      sh->cost0 = cost0;
     }
   }
   if (threadIdx.x == 0) {
@@ -232,6 +266,7 @@ __global__ void __launch_bounds__(kThreads)
   // Let the merge kernel launch; it waits for this grid before reading.
   pdl_launch_dependents();
   const int c0 = sh->c0, c1 = sh->c1, chunk = sh->chunk, b0 = sh->b0, off0 = sh->off0;
+  const int cost0 = sh->cost0;
   if (c0 >= c1 || b0 < 0) return;                 // whole CTA: no work
   const WaitCtl wc{&sh->abort, p.status, p.timeout_ns};
 
@@ -258,10 +293,10 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
     };
-    int cur_ph, cur_b, cur_g, nxt_ph, nxt_b, nxt_g;
+    // The first batch is translated before the loop; each next one a few
+    // copies into the current batch, so the first copy leaves at once.
+    int cur_ph, cur_b, cur_g, nxt_ph = -1, nxt_b = -1, nxt_g = 0;
     fetch(lane, cur_ph, cur_b, cur_g);
-    lw.skip(p, 32);
-    fetch(32 + lane, nxt_ph, nxt_b, nxt_g);
 
     int issued = 0, seg = 0, pb = -1, pg = -1;
     bool ok = true;
@@ -272,8 +307,10 @@ __global__ void __launch_bounds__(kThreads)
         cur_ph = nxt_ph;
         cur_b = nxt_b;
         cur_g = nxt_g;
+      }
+      if (j == 4) {
         lw.skip(p, 32);
-        fetch(c + 32 + lane, nxt_ph, nxt_b, nxt_g);
+        fetch(c - 4 + 32 + lane, nxt_ph, nxt_b, nxt_g);
       }
       const int phys = __shfl_sync(0xffffffffu, cur_ph, j);
       const int b = __shfl_sync(0xffffffffu, cur_b, j);
@@ -488,8 +525,10 @@ __global__ void __launch_bounds__(kThreads)
       if (threadIdx.x == 0) mbar_arrive(smem_addr(&sh->qempty[qs]));
       const bool last = (w.blk + cnt == w.nblk);
       const bool whole = (w.blk == 0) && last;
-      const int c_first = (w.flat - w.blk) / chunk;
-      const int part = static_cast<int>(blockIdx.x) - c_first;
+      // Part index = this CTA - the CTA holding block 0 of the run.  Only the
+      // first segment can continue a run: its block 0 sits at cost position
+      // cost0 - w.blk, in CTA (cost0 - w.blk) / chunk.
+      const int part = (w.blk > 0) ? static_cast<int>(blockIdx.x) - (cost0 - w.blk) / chunk : 0;
       for (int idx = threadIdx.x; idx < G * D; idx += kConsumers * 32) {
         const int r = idx / D;
         const int d = idx % D;
@@ -540,10 +579,15 @@ struct CombineParams {
 };
 
 // One warp per (sequence, query head): exact merge of the parts of a
-// sequence that was split over several CTAs.  Lane s holds part s's (max,
-// sum); the weights come from warp reductions and every part's row is loaded
-// before any is accumulated.  Sequences with one part were written by the
-// decode kernel; empty sequences get O = 0 and LSE = -inf here.
+// sequence that was split over several CTAs.  Everything the merge can need
+// is loaded at once, before any of it is used: the length, the part count,
+// every part's (max, sum) (lane s holds part s) and the O rows of the first
+// kPrefetch parts; the part count then selects among them (rows of parts
+// that were not written are never read into the sum).  So a merge costs one
+// round trip to memory; only sequences with more parts loop over the rest.
+// Sequences with one part were written by the decode kernel; empty
+// sequences get O = 0 and LSE = -inf here.
+constexpr int kPrefetch = 8;
 template <int D>
 __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineParams p) {
   pdl_wait_primary();
@@ -551,8 +595,25 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
   const int h = blockIdx.x * 4 + warp;
   const int b = blockIdx.y;
   if (h >= p.Hq) return;
-  int L = p.seq_lens[b];
-  L = L < 0 ? 0 : min(L, p.max_blocks * kBS);
+  const int G = p.Hq / p.Hkv;
+  const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.max_parts;
+  // ---- all independent loads first
+  const int L_raw = p.seq_lens[b];
+  const int np_raw = __ldcg(p.nparts + b * p.Hkv + h / G);
+  float m_lane = -INFINITY, l_lane = 0.f;
+  if (lane < p.max_parts) {
+    m_lane = __ldcg(p.ws_ml + (base + lane) * 2);
+    l_lane = __ldcg(p.ws_ml + (base + lane) * 2 + 1);
+  }
+  float v[kPrefetch][D / 32];
+#pragma unroll
+  for (int s = 0; s < kPrefetch; ++s) {
+    const float* src = p.ws_o + (base + min(s, p.max_parts - 1)) * D;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) v[s][e] = __ldcg(src + lane + 32 * e);
+  }
+  // ---- then decide
+  const int L = L_raw < 0 ? 0 : min(L_raw, p.max_blocks * kBS);
   __nv_bfloat16* dst = p.o + (static_cast<size_t>(b) * p.Hq + h) * D;
   if (L == 0) {
 #pragma unroll
@@ -560,13 +621,15 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
     if (lane == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(b) * p.Hq + h] = -INFINITY;
     return;
   }
-  const int G = p.Hq / p.Hkv;
-  const int np = min(p.nparts[b * p.Hkv + h / G], p.max_parts);
+  const int np = min(np_raw, p.max_parts);
   if (np <= 1) return;
-  const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.max_parts;
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < np; s0 += 32)
-    if (s0 + lane < np) M = fmaxf(M, p.ws_ml[(base + s0 + lane) * 2]);
+  if (lane >= np) {
+    m_lane = -INFINITY;
+    l_lane = 0.f;
+  }
+  // Parts beyond 32 (only with very long block tables) join the maximum here.
+  for (int s = 32 + lane; s < np; s += 32) m_lane = fmaxf(m_lane, __ldcg(p.ws_ml + (base + s) * 2));
+  float M = m_lane;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[D / 32];
@@ -574,32 +637,32 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
   for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
   float lsum = 0.f;
   if (M != -INFINITY) {
-    for (int s0 = 0; s0 < np; s0 += 32) {
-      const int cnt = min(32, np - s0);
-      float w = 0.f, lw = 0.f;
-      if (lane < cnt) {
-        w = ex2(p.ws_ml[(base + s0 + lane) * 2] - M);
-        lw = w * p.ws_ml[(base + s0 + lane) * 2 + 1];
-      }
+    // Weights of the first 32 parts from the values already in registers.
+    const float w = (lane < np) ? ex2(m_lane - M) : 0.f;
+    float lw = w * l_lane;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-      lsum += lw;
-      for (int s = 0; s < cnt; s += 4) {
-        float v[4][D / 32], ws[4];
+    for (int s = 0; s < kPrefetch; ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      if (s < np)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          ws[u] = __shfl_sync(0xffffffffu, w, min(s + u, 31));
-          const float* src = p.ws_o + (base + s0 + min(s + u, cnt - 1)) * D;
-#pragma unroll
-          for (int e = 0; e < D / 32; ++e) v[u][e] = src[lane + 32 * e];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (s + u < cnt)
-#pragma unroll
-            for (int e = 0; e < D / 32; ++e) acc[e] += ws[u] * v[u][e];
-      }
+        for (int e = 0; e < D / 32; ++e) acc[e] += ws * v[s][e];
     }
+    for (int s = kPrefetch; s < min(np, 32); ++s) {
+      const float ws = __shfl_sync(0xffffffffu, w, s);
+      const float* src = p.ws_o + (base + s) * D;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) acc[e] += ws * __ldcg(src + lane + 32 * e);
+    }
+    for (int s = 32; s < np; ++s) {
+      const float ws = ex2(__ldcg(p.ws_ml + (base + s) * 2) - M);
+      if (lane == 0) lw += ws * __ldcg(p.ws_ml + (base + s) * 2 + 1);
+      const float* src = p.ws_o + (base + s) * D;
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) acc[e] += ws * __ldcg(src + lane + 32 * e);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+    lsum = lw;
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
@@ -677,8 +740,9 @@ cudaError_t launch_t(const DecLaunch& a) {
 }  // namespace
 
 int decode_max_parts(int max_blocks_per_seq) {
-  // Every chunk holds at least kMinChunk block-heads, so the n blocks of
-  // one (sequence, KV head) meet at most ceil(n / kMinChunk) + 1 chunks.
+  // The start cost of a run lies before its block 0, and every later chunk
+  // covers at least kMinChunk of its blocks, so the n blocks of one
+  // (sequence, KV head) meet at most ceil(n / kMinChunk) + 1 chunks.
   return (max_blocks_per_seq + kMinChunk - 1) / kMinChunk + 1;
 }
 
