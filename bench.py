@@ -47,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu summaries (profiles/), taken on this workload; None once a kernel changes
 # until it is captured again.  Decode: main kernel + merge kernel.
 TRAFFIC_FWD = 67190784 + 9360384
-TRAFFIC_DEC = None
+TRAFFIC_DEC = (132292096 + 3670272) + (3272704 + 0)
 
 
 def peaks():
