@@ -264,6 +264,41 @@ def build_sets(rank, device):
     return c, dc, host, sets
 
 
+def fwd_config_table(attn, device, steps, peak):
+    """Forward TFLOP/s on the other prefill configs (GPT-2-small-shaped, d = 64;
+    long context, N = 16384), timed like the main workload: CUDA events over
+    `steps` launches after 3 warm-ups, input sets rotated so that they exceed L2."""
+    out = {}
+    for name in ("gpt2_small", "long_context"):
+        c = workloads.PREFILL_CONFIGS[name]
+        nsets = 3 if name == "gpt2_small" else 1    # 3 x 50 MB, or one 268 MB set: > L2 either way
+        sets = []
+        for i in range(nsets):
+            q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"] + 100 * i,
+                                               std=c["std"], key_offset=c["key_offset"])
+            sets.append((q.to(device), k.to(device), v.to(device)))
+        scale = workloads.default_scale(c["d"])
+        o = torch.empty_like(sets[0][0])
+        lse = torch.empty(sets[0][0].shape[:3], dtype=torch.float32, device=device)
+        for i in range(3):
+            attn.attn_fwd(*sets[i % nsets], causal=True, scale=scale, o=o, lse=lse)
+        stream = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(steps):
+            attn.attn_fwd(*sets[i % nsets], causal=True, scale=scale, o=o, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        tflops = fwd_flops(c) / (ms / 1e3) / 1e12
+        out[name] = {"shape": "B%d Hq%d Hkv%d N%d d%d causal" % (c["B"], c["Hq"], c["Hkv"], c["N"], c["d"]),
+                     "ms": ms, "tflops": tflops, "frac": tflops / peak}
+        del sets, o, lse
+    return out
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_47_gb300 as attn
 
@@ -363,6 +398,8 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
     clock.stop()
+    pk_all, _ = peaks()
+    fwd_configs = fwd_config_table(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
 
     # ---- max over ranks
     total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
@@ -398,6 +435,9 @@ def run_gpu(args, rank, world, local_rank):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "note": "fwd flops over the whole step: pinned h2d of q,k,v and of the "
                             "decode query/table/lengths, both ops, d2h of all outputs"},
+            "fwd_configs": dict(fwd_configs, **{FWD_CFG: {
+                "shape": "B4 Hq12 Hkv2 N4096 d128 causal", "ms": fwd_sum / K,
+                "tflops": achieved_fwd, "frac": achieved_fwd / pk["bf16_tflops"]}}),
             "gpu_launches": 3 * K,
             "clocks": clock.summary(wall0, wall1),
         }
