@@ -212,6 +212,7 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.d = d;
   a.causal = causal != 0;
   a.scale = scale;
+  a.sms = dev->sms;
   a.status = dev->status;
   a.timeout_ns = g_timeout_ns;
   a.stream = static_cast<cudaStream_t>(stream);

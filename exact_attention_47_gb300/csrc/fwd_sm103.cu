@@ -75,9 +75,10 @@ struct FwdLayout {
 };
 
 struct FwdBarriers {
-  uint64_t q_full;
+  uint64_t q_full[2], q_empty[2];     // Q tile x of the current work unit / free again
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t o_free[2];                 // O_X read out by the epilogue of the previous unit
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort;
@@ -86,7 +87,7 @@ struct FwdBarriers {
 struct FwdParams {
   void* o;
   float* lse;
-  int N, Hq, Hkv, group, num_q_blocks, bh_total;
+  int N, Hq, Hkv, group, num_q_blocks, bh_total, num_units;
   float scale_log2;
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -109,18 +110,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Heaviest (last, for causal) query blocks first across the whole grid.
-  const int qblk = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x) / p.bh_total;
-  const int bh = static_cast<int>(blockIdx.x) % p.bh_total;
-  const int zq = bh;                                   // b * Hq + h
-  const int zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+  // Persistent CTAs: work unit k (one 256-row query block of one (batch,
+  // head)) in heaviest-first order (last query blocks first, for causal);
+  // CTA c takes unit c of the first band of gridDim.x units, then walks the
+  // bands in alternating directions so heavy and light units pair up.
+  const int grid = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  auto unit_at = [&](int band) {
+    return band * grid + ((band & 1) ? grid - 1 - cta : cta);
+  };
   const int kv_total = (p.N + kBN - 1) / kBN;
-  // K/V tiles each query tile needs; the diagonal tile of tile X is 2*qblk + X.
-  const int nA = CAUSAL ? min(2 * qblk + 1, kv_total) : kv_total;
-  const int nB = CAUSAL ? min(2 * qblk + 2, kv_total) : kv_total;
+  struct Unit {
+    int qblk, zq, zkv, nA, nB;
+  };
+  auto unit_info = [&](int k) {
+    Unit u;
+    u.qblk = p.num_q_blocks - 1 - k / p.bh_total;
+    const int bh = k % p.bh_total;
+    u.zq = bh;                                         // b * Hq + h
+    u.zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+    // K/V tiles each query tile needs; the diagonal tile of tile X is 2*qblk + X.
+    u.nA = CAUSAL ? min(2 * u.qblk + 1, kv_total) : kv_total;
+    u.nB = CAUSAL ? min(2 * u.qblk + 2, kv_total) : kv_total;
+    return u;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar->q_full), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_addr(&bar->q_full[x]), 1);
+      mbar_init(smem_addr(&bar->q_empty[x]), 1);
+      mbar_init(smem_addr(&bar->o_free[x]), 4);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(smem_addr(&bar->k_full[s]), 1);
       mbar_init(smem_addr(&bar->v_full[s]), 1);
@@ -153,31 +173,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      const uint32_t qf = smem_addr(&bar->q_full);
-      mbar_arrive_expect_tx(qf, kTiles * L::kQTile);
-      for (int x = 0; x < kTiles; ++x)
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sQ + x * L::kQTile + c * L::kQChunk, &tq, qf, c * 64,
-                      qblk * kRowsPerCta + x * kBM, zq);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < nB; ++j) {
-        const int st = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!mbar_wait(smem_addr(&bar->k_empty[st]), ph ^ 1, wc)) break;
-        const uint32_t kf = smem_addr(&bar->k_full[st]);
-        mbar_arrive_expect_tx(kf, L::kKV);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sK + st * L::kKV + c * L::kKVChunk, &tk, kf, c * 64, j * kBN, zkv);
-        ++k_issued;
-        if (!mbar_wait(smem_addr(&bar->v_empty[st]), ph ^ 1, wc)) break;
-        const uint32_t vf = smem_addr(&bar->v_full[st]);
-        mbar_arrive_expect_tx(vf, L::kKV);
-        for (int c = 0; c < L::kChunks; ++c)
-          tma_load_3d(sV + st * L::kKV + c * L::kKVChunk, &tv, vf, c * 64, j * kBN, zkv);
-        ++v_issued;
+      int kv_issued = 0, k_issued = 0, v_issued = 0, units = 0;
+      bool ok = true;
+      for (int band = 0; ok; ++band) {
+        const int k = unit_at(band);
+        if (k >= p.num_units) break;
+        const Unit u = unit_info(k);
+        // Q tile x of this unit, once the last S MMA of the previous unit has
+        // read it.  Order: Q_A, K_0, Q_B, V_0, K_1, ...: the first S MMA of
+        // the unit needs only Q_A and K_0, which can land while the previous
+        // unit's last tile-B MMAs still read Q_B.
+        auto load_q = [&](int x) {
+          if (units > 0 && !(ok = mbar_wait(smem_addr(&bar->q_empty[x]), (units - 1) & 1, wc))) return;
+          const uint32_t qf = smem_addr(&bar->q_full[x]);
+          mbar_arrive_expect_tx(qf, L::kQTile);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sQ + x * L::kQTile + c * L::kQChunk, &tq, qf, c * 64,
+                        u.qblk * kRowsPerCta + x * kBM, u.zq);
+        };
+        load_q(0);
+        // K/V tiles: one stage ring for the whole CTA, across units.
+        for (int j = 0; j < u.nB && ok; ++j) {
+          const int g = kv_issued + j;
+          const int st = g % L::kStages;
+          const uint32_t ph = (g / L::kStages) & 1;
+          if (!(ok = mbar_wait(smem_addr(&bar->k_empty[st]), ph ^ 1, wc))) break;
+          const uint32_t kf = smem_addr(&bar->k_full[st]);
+          mbar_arrive_expect_tx(kf, L::kKV);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sK + st * L::kKV + c * L::kKVChunk, &tk, kf, c * 64, j * kBN, u.zkv);
+          ++k_issued;
+          if (j == 0) {
+            load_q(1);
+            if (!ok) break;
+          }
+          if (!(ok = mbar_wait(smem_addr(&bar->v_empty[st]), ph ^ 1, wc))) break;
+          const uint32_t vf = smem_addr(&bar->v_full[st]);
+          mbar_arrive_expect_tx(vf, L::kKV);
+          for (int c = 0; c < L::kChunks; ++c)
+            tma_load_3d(sV + st * L::kKV + c * L::kKVChunk, &tv, vf, c * 64, j * kBN, u.zkv);
+          ++v_issued;
+        }
+        kv_issued += u.nB;
+        ++units;
       }
       // Every copy issued must have landed before the CTA may exit.
-      mbar_wait(qf, 0, wc, true);
+      if (units > 0)
+        for (int x = 0; x < kTiles; ++x) mbar_wait(smem_addr(&bar->q_full[x]), (units - 1) & 1, wc, true);
       for (int st = 0; st < L::kStages; ++st) {
         const int nk = k_issued > st ? (k_issued - 1 - st) / L::kStages + 1 : 0;
         const int nv = v_issued > st ? (v_issued - 1 - st) / L::kStages + 1 : 0;
@@ -195,26 +237,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kF = smem_addr(&bar->k_full[0]);
       const uint32_t vF = smem_addr(&bar->v_full[0]);
       const uint32_t pF = smem_addr(&bar->p_full[0]);
-      auto kfull = [&](int jj) { return kF + 8u * (jj % L::kStages); };
-      auto vfull = [&](int jj) { return vF + 8u * (jj % L::kStages); };
-      auto ph = [&](int jj) { return static_cast<uint32_t>((jj / L::kStages) & 1); };
+      // K/V tile jj of the current unit is fill g0 + jj of the CTA's stage ring.
+      int g0 = 0;
+      auto kfull = [&](int jj) { return kF + 8u * ((g0 + jj) % L::kStages); };
+      auto vfull = [&](int jj) { return vF + 8u * ((g0 + jj) % L::kStages); };
+      auto ph = [&](int jj) { return static_cast<uint32_t>(((g0 + jj) / L::kStages) & 1); };
+      // P_X(jj) of the current unit is completion pX0 + jj of p_full[X].
+      int pa0 = 0, pb0 = 0;
+      auto ppar = [&](int x, int jj) { return static_cast<uint32_t>(((x ? pb0 : pa0) + jj) & 1); };
       // A dependency that was probed ready is not waited on again.
       auto ensure = [&](uint32_t b, uint32_t parity, uint32_t probed) -> bool {
         return __all_sync(0xffffffffu, probed != 0u) || mbar_wait_warp(b, parity, wc);
       };
       // Next group's probes: issued before the last two MMAs of a group.
       uint32_t rA = 0, rB = 0;
-      int probe_kind = 0, probe_j = 0;             // 1: PV (P, V)  2: S (K)
+      int probe_kind = 0, probe_x = 0, probe_j = 0;   // 1: PV (P, V)  2: S (K)
       auto do_probes = [&]() {
         if (probe_kind == 1) {
-          rA = mbar_probe(pF + 8u * static_cast<uint32_t>(probe_j >> 16), probe_j & 1);
-          rB = mbar_probe(vfull(probe_j & 0xffff), ph(probe_j & 0xffff));
+          rA = mbar_probe(pF + 8u * static_cast<uint32_t>(probe_x), ppar(probe_x, probe_j));
+          rB = mbar_probe(vfull(probe_j), ph(probe_j));
         } else if (probe_kind == 2) {
           rA = mbar_probe(kfull(probe_j), ph(probe_j));
         }
       };
       auto group_s = [&](int x, int jj) {
-        const int st = jj % L::kStages;
+        const int st = (g0 + jj) % L::kStages;
         const uint32_t qbase = sQ + x * L::kQTile;
         const uint32_t kbase = sK + st * L::kKV;
         const uint32_t dS = tmem + (x ? L::kColS1 : L::kColS0);
@@ -228,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit_warp(smem_addr(&bar->s_full[x]));
       };
       auto group_pv = [&](int x, int jj) {
-        const int st = jj % L::kStages;
+        const int st = (g0 + jj) % L::kStages;
         const uint32_t vbase = sV + st * L::kKV;
         const uint32_t aP = tmem + (x ? L::kColS1 : L::kColS0);
         const uint32_t dO = tmem + (x ? L::kColO1 : L::kColO0);
@@ -240,61 +287,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts_warp(dO, aP + kk * 8, bd, kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
         }
       };
-      // Schedule (each group probes what the next one needs):
+      // Per unit (each group probes what the next one needs):
       //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
-      bool ok = mbar_wait_warp(smem_addr(&bar->q_full), 0, wc) && mbar_wait_warp(kfull(0), 0, wc);
-      if (ok) {
-        tc_fence_after();
-        probe_kind = 0;
-        group_s(0, 0);
-        probe_kind = 1;                            // PV_A(0): P_A(0), V_0
-        probe_j = 0;
-        group_s(1, 0);
-        umma_commit_warp(smem_addr(&bar->k_empty[0]));
-      }
-      for (int j = 0; j < nB && ok; ++j) {
-        const int st = j % L::kStages;
-        if (j < nA) {
-          // PV_A(j)
-          if (!(ok = ensure(pF, j & 1, rA) && ensure(vfull(j), ph(j), rB))) break;
+      // The first P V of a tile overwrites O_X, so it waits until the
+      // epilogue of the previous unit has read O_X out; the last S group of
+      // a tile releases its Q tile for the next unit's load.
+      bool ok = true;
+      int units = 0;
+      for (int band = 0; ok; ++band) {
+        const int k = unit_at(band);
+        if (k >= p.num_units) break;
+        const Unit u = unit_info(k);
+        const int nA = u.nA, nB = u.nB;
+        const uint32_t upar = static_cast<uint32_t>(units & 1);
+        ok = mbar_wait_warp(smem_addr(&bar->q_full[0]), upar, wc) &&
+             mbar_wait_warp(kfull(0), ph(0), wc);
+        if (ok) {
           tc_fence_after();
-          probe_kind = (j + 1 < nA) ? 2 : 0;       // S_A(j+1): K_{j+1}
-          probe_j = j + 1;
-          group_pv(0, j);
-          if (j == nA - 1) umma_commit_warp(smem_addr(&bar->o_done[0]));
-          if (j + 1 < nA) {
-            // S_A(j+1)
-            if (!(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+          probe_kind = 0;
+          group_s(0, 0);
+          if (nA == 1) umma_commit_warp(smem_addr(&bar->q_empty[0]));
+          ok = mbar_wait_warp(smem_addr(&bar->q_full[1]), upar, wc);
+        }
+        if (ok) {
+          tc_fence_after();
+          probe_kind = 1;                          // PV_A(0): P_A(0), V_0
+          probe_x = 0;
+          probe_j = 0;
+          group_s(1, 0);
+          if (nB == 1) umma_commit_warp(smem_addr(&bar->q_empty[1]));
+          umma_commit_warp(smem_addr(&bar->k_empty[g0 % L::kStages]));
+        }
+        for (int j = 0; j < nB && ok; ++j) {
+          const int st = (g0 + j) % L::kStages;
+          if (j < nA) {
+            // PV_A(j)
+            if (!(ok = ensure(pF, ppar(0, j), rA) && ensure(vfull(j), ph(j), rB))) break;
+            if (j == 0 && units > 0 && !(ok = mbar_wait_warp(smem_addr(&bar->o_free[0]), upar ^ 1, wc))) break;
             tc_fence_after();
-            probe_kind = 1;                        // PV_B(j): P_B(j), V_j (known)
-            probe_j = (1 << 16) | j;
-            group_s(0, j + 1);
-            rB = 1;
+            probe_kind = (j + 1 < nA) ? 2 : 0;     // S_A(j+1): K_{j+1}
+            probe_j = j + 1;
+            group_pv(0, j);
+            if (j == nA - 1) umma_commit_warp(smem_addr(&bar->o_done[0]));
+            if (j + 1 < nA) {
+              // S_A(j+1)
+              if (!(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+              tc_fence_after();
+              probe_kind = 1;                      // PV_B(j): P_B(j), V_j (known)
+              probe_x = 1;
+              probe_j = j;
+              group_s(0, j + 1);
+              if (j + 1 == nA - 1) umma_commit_warp(smem_addr(&bar->q_empty[0]));
+              rB = 1;
+            } else {
+              rA = mbar_probe(pF + 8u, ppar(1, j));
+              rB = 1;
+            }
           } else {
-            rA = mbar_probe(pF + 8u, j & 1);
-            rB = 1;
+            rA = mbar_probe(pF + 8u, ppar(1, j));
+            rB = mbar_probe(vfull(j), ph(j));
           }
-        } else {
-          rA = mbar_probe(pF + 8u, j & 1);
-          rB = mbar_probe(vfull(j), ph(j));
-        }
-        // PV_B(j)
-        if (!(ok = ensure(pF + 8u, j & 1, rA) && ensure(vfull(j), ph(j), rB))) break;
-        tc_fence_after();
-        probe_kind = (j + 1 < nB && j + 1 >= nA) ? 2 : 0;   // S_B(j+1) needs K_{j+1} if S_A did not test it
-        probe_j = j + 1;
-        group_pv(1, j);
-        umma_commit_warp(smem_addr(&bar->v_empty[st]));
-        if (j == nB - 1) umma_commit_warp(smem_addr(&bar->o_done[1]));
-        if (j + 1 < nB) {
-          // S_B(j+1)
-          if (j + 1 >= nA && !(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+          // PV_B(j)
+          if (!(ok = ensure(pF + 8u, ppar(1, j), rA) && ensure(vfull(j), ph(j), rB))) break;
+          if (j == 0 && units > 0 && !(ok = mbar_wait_warp(smem_addr(&bar->o_free[1]), upar ^ 1, wc))) break;
           tc_fence_after();
-          probe_kind = (j + 1 < nA) ? 1 : 0;       // PV_A(j+1): P_A(j+1), V_{j+1}
+          probe_kind = (j + 1 < nB && j + 1 >= nA) ? 2 : 0;   // S_B(j+1) needs K_{j+1} if S_A did not test it
           probe_j = j + 1;
-          group_s(1, j + 1);
-          umma_commit_warp(smem_addr(&bar->k_empty[(j + 1) % L::kStages]));
+          group_pv(1, j);
+          umma_commit_warp(smem_addr(&bar->v_empty[st]));
+          if (j == nB - 1) umma_commit_warp(smem_addr(&bar->o_done[1]));
+          if (j + 1 < nB) {
+            // S_B(j+1)
+            if (j + 1 >= nA && !(ok = ensure(kfull(j + 1), ph(j + 1), rA))) break;
+            tc_fence_after();
+            probe_kind = (j + 1 < nA) ? 1 : 0;     // PV_A(j+1): P_A(j+1), V_{j+1}
+            probe_x = 0;
+            probe_j = j + 1;
+            group_s(1, j + 1);
+            if (j + 1 == nB - 1) umma_commit_warp(smem_addr(&bar->q_empty[1]));
+            umma_commit_warp(smem_addr(&bar->k_empty[(g0 + j + 1) % L::kStages]));
+          }
         }
+        g0 += nB;
+        pa0 += nA;
+        pb0 += nB;
+        ++units;
+        probe_kind = 0;
+        rA = rB = 0;
       }
       // All issued MMAs must retire before TMEM is released.
       umma_commit_warp(smem_addr(&bar->mma_final));
@@ -315,20 +394,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = warp >> 2;                       // query tile of this warpgroup
     const int quarter = warp & 3;                  // TMEM lane quarter of this warp
     const int row = quarter * 32 + lane;           // row within the tile = TMEM lane
-    const int qrow = qblk * kRowsPerCta + x * kBM + row;
-    const int n_kv = x ? nB : nA;
-    const int diag = 2 * qblk + x;                 // causal: the tile holding key == row
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t colS = x ? L::kColS1 : L::kColS0;
     const uint32_t colO = x ? L::kColO1 : L::kColO0;
     const float sl2 = p.scale_log2;
+    bool ok = true;
+    int sx0 = 0;                                   // S_X tiles consumed in earlier units
+    int units = 0;
+    for (int band = 0; ok; ++band) {
+    const int k = unit_at(band);
+    if (k >= p.num_units) break;
+    const Unit u = unit_info(k);
+    const int qrow = u.qblk * kRowsPerCta + x * kBM + row;
+    const int n_kv = x ? u.nB : u.nA;
+    const int diag = 2 * u.qblk + x;               // causal: the tile holding key == row
+    const int zq = u.zq;
     float m = 0.f;                                 // stabiliser in use (exp2 domain)
     float l = 0.f;                                 // denominator relative to m (fp32 terms)
     float lr = 0.f;                                // same, bf16-rounded terms
-    bool ok = true;
 
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(smem_addr(&bar->s_full[x]), j & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(smem_addr(&bar->s_full[x]), static_cast<uint32_t>(sx0 + j) & 1u, wc)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       uint32_t r0[32], r1[32], r2[32], r3[32];
       ATTN47_TMEM_LD32(tl + colS + 0, r0);
@@ -442,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ epilogue
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && mbar_wait_warp(smem_addr(&bar->o_done[x]), 0, wc)) {
+    if (ok && mbar_wait_warp(smem_addr(&bar->o_done[x]), static_cast<uint32_t>(units & 1), wc)) {
       tc_fence_after();
       const float inv_l = 1.f / lr;
       const bool in_range = qrow < p.N;
@@ -466,6 +555,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (in_range && p.lse != nullptr)
         p.lse[static_cast<size_t>(zq) * p.N + qrow] = (m + __log2f(l)) * kLn2;
+      // O_X has been read out: the next unit's first P V may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->o_free[x]));
+    } else {
+      ok = false;
+    }
+    sx0 += n_kv;
+    ++units;
     }
     tc_fence_before();
     named_barrier_sync(1, kThreads);
@@ -487,10 +585,12 @@ cudaError_t launch_t(const FwdLaunch& a) {
   p.group = a.Hq / a.Hkv;
   p.num_q_blocks = (a.N + kRowsPerCta - 1) / kRowsPerCta;
   p.bh_total = a.B * a.Hq;
+  p.num_units = p.num_q_blocks * p.bh_total;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  const unsigned grid = static_cast<unsigned>(p.num_q_blocks) * static_cast<unsigned>(p.bh_total);
+  // Persistent: one CTA per SM (shared memory allows one), each walking units.
+  const unsigned grid = static_cast<unsigned>(min(p.num_units, a.sms > 0 ? a.sms : 1));
   kern<<<grid, kThreads, L::kSmem, a.stream>>>(*a.tq, *a.tk, *a.tv, p);
   return cudaGetLastError();
 }

@@ -15,6 +15,7 @@ struct FwdLaunch {
   int B, Hq, Hkv, N, d;
   bool causal;
   float scale;
+  int sms;                 // SMs of the device (persistent grid)
   unsigned int* status;    // device status word
   unsigned long long timeout_ns;
   cudaStream_t stream;
