@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
 # ncu summaries (profiles/), taken on this workload; None once a kernel changes
 # until it is captured again.  Decode: main kernel + merge kernel.
-TRAFFIC_FWD = None
+TRAFFIC_FWD = 67189504 + 7851008
 TRAFFIC_DEC = (132292096 + 3670272) + (3272704 + 0)
 
 

@@ -57,6 +57,26 @@ def test_small_shapes(shape, causal):
     assert_attn_close(o, lse, *ref(q, k, v, causal, scale), what=str(shape))
 
 
+# Many more (query block, head) units than SMs: every CTA walks several units,
+# with ragged query and key tails, so the barrier phases that continue from
+# one unit to the next are exercised.  All output elements are compared.
+WALKS = [  # B, Hq, Hkv, N, d
+    (4, 48, 8, 700, 128), (2, 64, 64, 333, 64), (1, 160, 16, 260, 128),
+]
+
+
+@pytest.mark.parametrize("shape", WALKS, ids=lambda s: "B%dHq%dHkv%dN%dd%d" % s)
+@pytest.mark.parametrize("causal", [False, True])
+def test_units_walked_per_cta(shape, causal):
+    B, Hq, Hkv, N, d = shape
+    q, k, v = workloads.prefill_inputs(B, Hq, Hkv, N, d, seed=300 + N + d)
+    scale = workloads.default_scale(d)
+    o, lse = run(q, k, v, causal, scale)
+    o2, lse2 = run(q, k, v, causal, scale)          # a second launch starts from scratch
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert_attn_close(o, lse, *ref(q, k, v, causal, scale), what=str(shape))
+
+
 @pytest.mark.parametrize("scale", [0.02, 0.3, 1.0])
 def test_scales_and_wide_logits(scale):
     """Wide, peaky logits (q, k with std 1.5 and per-key offsets).  V keeps
