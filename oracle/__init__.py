@@ -19,6 +19,7 @@ No function is "parity unpinned".
 
 from .definitions import (  # noqa: F401
     attention,
+    attention_backward,
     attention_online,
     combine_partials,
     decode_paged,

@@ -103,6 +103,48 @@ def attention(q, k, v, scale, causal, rows=None):
     return o, lse
 
 
+def attention_backward(q, k, v, do, scale, causal):
+    """Gradients of exact attention with respect to q, k and v.
+
+    The forward is the plain definition of ``attention`` ("Advanced attention
+    mechanisms – II", section "Why?"); section "Flash Attention" keeps the
+    softmax statistics so that the backward pass can recompute the attention
+    matrix instead of storing it.  This is the chain rule of that definition
+    written out, with upstream gradient ``do`` = dL/dO:
+
+        P    = softmax(s) over the allowed keys,  s = scale * Q K^T
+        dV   = P^T dO                      (O = P V)
+        dP   = dO V^T
+        dS_ij = P_ij * (dP_ij - sum_k P_ik dP_ik)   (Jacobian of the row softmax)
+        dQ   = scale * dS K,   dK = scale * dS^T Q
+
+    Disallowed (masked) entries have P = 0 and so no gradient.  With GQA the
+    K/V gradients of a KV head are summed over the query heads that read it.
+    Returns (dq [B,Hq,N,d], dk [B,Hkv,N,d], dv [B,Hkv,N,d]) in fp64.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if Hq % Hkv != 0:
+        raise ValueError("Hq must be a multiple of Hkv")
+    group = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // group
+            s = score_matrix(q[b, h], k[b, g], scale)
+            allowed = _causal_allowed(np.arange(N), k.shape[2]) if causal else np.ones_like(s, dtype=bool)
+            p, _, _ = softmax_probs(s, allowed)
+            dv[b, g] += p.T @ do[b, h]
+            dp = do[b, h] @ v[b, g].T
+            ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))
+            dq[b, h] = float(scale) * (ds @ k[b, g])
+            dk[b, g] += float(scale) * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
 def attention_online(q, k, v, scale, causal, tile):
     """Tile-by-tile attention with the running-max / running-sum softmax.
 
