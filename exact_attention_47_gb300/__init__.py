@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     BLOCK_SIZE,
     AttnError,
     abi_version,
+    attn_bwd,
+    attn_bwd_workspace_size,
     attn_decode_paged,
     attn_decode_paged_noalloc,
     attn_decode_paged_workspace_size,

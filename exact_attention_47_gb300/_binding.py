@@ -26,6 +26,9 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float, _P]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                      _P, ctypes.c_size_t, _P]),
     "attn_decode_paged_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode_paged": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                                _P, _P, _P, ctypes.c_size_t, _P]),
@@ -137,6 +140,48 @@ def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None, return_lse=True
                       1 if causal else 0, float(scale), _stream_handle(stream))
     _check("attn_fwd", st)
     return o, lse
+
+
+def attn_bwd_workspace_size(B, Hq, N):
+    return int(load_library().attn_bwd_workspace_size(B, Hq, N))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal=True, scale=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients of attn_fwd.  q/o/dout [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 and
+    lse [B,Hq,N] fp32 (attn_fwd's outputs for the same inputs), on the GPU.
+
+    Returns (dq [B,Hq,N,d], dk [B,Hkv,N,d], dv [B,Hkv,N,d]) bf16.
+    """
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need_cuda(name, t, torch.bfloat16)
+        if t.dim() != 4:
+            raise ValueError("%s must be 4-D [B, H, N, d]" % name)
+    _need_cuda("lse", lse, torch.float32)
+    B, Hq, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, N, d] matching q")
+    if o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (B, Hq, N):
+        raise ValueError("o and dout must have q's shape, lse [B, Hq, N]")
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        _need_cuda(name, t, torch.bfloat16)
+        if t.shape != ref.shape:
+            raise ValueError("%s has the wrong shape" % name)
+    need = attn_bwd_workspace_size(B, Hq, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                      _ptr(dv), B, Hq, Hkv, N, d, 1 if causal else 0, float(scale), _ptr(workspace),
+                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check("attn_bwd", st)
+    return dq, dk, dv
 
 
 def attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq):

@@ -12,6 +12,7 @@
 
 #include "attn47.h"
 #include "decode_sm103.h"
+#include "bwd_sm103.h"
 #include "fwd_sm103.h"
 #include "ptx.cuh"
 
@@ -217,6 +218,79 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   a.timeout_ns = g_timeout_ns;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_result(attn47::launch_fwd_sm103(a), "attn_fwd");
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int N) {
+  if (B <= 0 || Hq <= 0 || N <= 0) return 0;
+  return attn47::bwd_workspace_bytes(B, Hq, N);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                       int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  if (B < 0 || N < 0 || Hq < 1 || Hkv < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy B >= 0, N >= 0, Hq >= 1, Hkv >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (B == 0 || N == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, lse, dout, dq, dk and dv must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, dout, dq, dk and dv must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return fail(ATTN_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const size_t need = attn47::bwd_workspace_bytes(B, Hq, N);
+  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace must be non-null");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (static_cast<long long>(B) * Hq * tiles > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(attn47::bwd_box_rows()), 1};
+  const cuuint64_t dq_dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                 static_cast<cuuint64_t>(B) * Hq};
+  const cuuint64_t dkv_dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                  static_cast<cuuint64_t>(B) * Hkv};
+  alignas(64) CUtensorMap tq, tk, tv, tdo;
+  if ((st = encode_bf16(&tq, q, 3, dq_dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tk, k, 3, dkv_dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tv, v, 3, dkv_dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tdo, dout, 3, dq_dims, box)) != ATTN_OK) return st;
+
+  attn47::BwdLaunch a;
+  a.tq = &tq;
+  a.tk = &tk;
+  a.tv = &tv;
+  a.tdo = &tdo;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.causal = causal != 0;
+  a.scale = scale;
+  a.workspace = static_cast<float*>(workspace);
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_bwd_sm103(a), "attn_bwd");
 }
 
 size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq) {

@@ -1,0 +1,584 @@
+// Exact attention backward for sm_103a: dQ, dK, dV by recomputation.
+//
+// "Advanced attention mechanisms – II", section "Flash Attention": the
+// forward keeps only O and the softmax statistics (the LSE) so that the
+// backward pass can recompute the attention matrix tile by tile instead of
+// reading a stored one.  With s = scale * Q K^T and P = exp(s - lse):
+//     D_i  = sum_c dO_ic O_ic            (= sum_j P_ij dP_ij)
+//     dV   = P^T dO,   dP = dO V^T,   dS = P * (dP - D)
+//     dQ   = scale * dS K,   dK = scale * dS^T Q
+// The score matrix never reaches HBM; with GQA the K/V gradients of a KV
+// head are accumulated over its query heads inside one CTA.
+//
+// Three kernels, in stream order:
+//   attn_bwd_rowdot_kernel     D and lse * log2(e) per query row (HBM-bound)
+//   attn_bwd_dq_kernel         one 128-row query tile per CTA, loops over K/V
+//   attn_bwd_dkdv_kernel       one 128-key tile per CTA, loops over the query
+//                              tiles of every query head of its group
+// Both tile kernels: warps 0-3 compute (one TMEM lane = one row per thread),
+// warp 4 the TMA producer, warp 5 the MMA issuer and TMEM owner.  All
+// contractions are tcgen05 MMAs with fp32 accumulators in TMEM; P and dS go
+// back into TMEM as bf16 and feed the next MMAs as their A operand.
+#include <cuda_runtime.h>
+
+#include "bwd_sm103.h"
+#include "ptx.cuh"
+
+namespace attn47 {
+namespace {
+
+constexpr int kTile = 128;          // query rows / keys per tile (= TMEM lanes)
+constexpr int kThreads = 192;
+constexpr int kWarpLoad = 4;
+constexpr int kWarpMma = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kChunks = D / 64;           // 128-byte swizzle atoms per row
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kChunkBytes = kTile * 128;  // one 64-column box of a tile
+  static constexpr int kStages = 2;
+  // dQ kernel: Q, dO once; K, V per stage.  dK/dV kernel: K, V once; Q, dO
+  // (+ 128 lse2 and 128 D values) per stage.  Same sizes either way.
+  static constexpr int kOffA = 0;                                  // Q (dq) | K (dkdv)
+  static constexpr int kOffB = kOffA + kTileBytes;                 // dO (dq) | V (dkdv)
+  static constexpr int kOffS0 = kOffB + kTileBytes;                // stage tiles
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kOffVec = kOffS0 + kStages * kStageBytes;   // [stage][lse2 | D][128]
+  static constexpr int kVecBytes = kStages * 2 * kTile * 4;
+  static constexpr int kOffBar = kOffVec + kVecBytes;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
+};
+
+struct BwdBarriers {
+  uint64_t once_full;                 // the tiles loaded once per CTA
+  uint64_t st_full[2], st_empty[2];   // per-stage tiles (and vectors)
+  uint64_t s_full;                    // S and dP of a step are in TMEM
+  uint64_t p_full;                    // the compute warps wrote P / dS
+  uint64_t done;                      // last accumulating MMA completed
+  uint64_t mma_final;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(BwdBarriers) <= 256, "barrier block");
+
+// ------------------------------------------------------------------ row dot
+// D[r] = sum_c dO[r, c] * O[r, c] and lse2[r] = lse[r] * log2(e) for the
+// query rows of every (batch, head), rows padded to whole tiles with zeros.
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_rowdot_kernel(const BwdParams p) {
+  const int warps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
+  for (long long r = static_cast<long long>(blockIdx.x) * warps + (threadIdx.x >> 5); r < rows;
+       r += static_cast<long long>(gridDim.x) * warps) {
+    const int bh = static_cast<int>(r / p.n_pad);
+    const int n = static_cast<int>(r % p.n_pad);
+    float dsum = 0.f, lse2 = 0.f;
+    if (n < p.N) {
+      const size_t base = (static_cast<size_t>(bh) * p.N + n) * D;
+      constexpr int kPer = D / 32;                 // bf16 elements per lane (2 or 4)
+      const __nv_bfloat16* po = p.o + base + lane * kPer;
+      const __nv_bfloat16* pd = p.dout + base + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) dsum += __bfloat162float(po[e]) * __bfloat162float(pd[e]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      lse2 = p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e;
+    }
+    if (lane == 0) {
+      p.ws_d[r] = dsum;
+      p.ws_lse2[r] = lse2;
+    }
+  }
+}
+
+// Four 32-column chunks of two TMEM rows (a, b) -> callback on the fp32
+// values of each chunk; after every two chunks the callback's 32 packed bf16
+// words are stored over columns [32 * half, +32) of a, which were loaded
+// already (packed pairs fill columns half as fast as they are read).
+#define ATTN47_BWD_ROW_LOOP(TA, TB, BODY)                                                      \
+  _Pragma("unroll") for (int half = 0; half < 2; ++half) {                                     \
+    uint32_t pk[32];                                                                           \
+    _Pragma("unroll") for (int sub = 0; sub < 2; ++sub) {                                      \
+      const int chunk = half * 2 + sub;                                                        \
+      uint32_t ra[32], rb[32];                                                                 \
+      ATTN47_TMEM_LD32((TA) + chunk * 32, ra);                                                 \
+      ATTN47_TMEM_LD32((TB) + chunk * 32, rb);                                                 \
+      ATTN47_TMEM_LD_WAIT(ra);                                                                 \
+      ATTN47_TMEM_LD_WAIT(rb);                                                                 \
+      _Pragma("unroll") for (int c2 = 0; c2 < 16; ++c2) { BODY }                               \
+    }                                                                                          \
+    ATTN47_TMEM_ST32((TA) + half * 32, pk);                                                    \
+  }
+
+// ------------------------------------------------------------------- dQ
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                       const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
+  const uint32_t sQ = smem_addr(smem + L::kOffA);
+  const uint32_t sDO = smem_addr(smem + L::kOffB);
+  const uint32_t sSt = smem_addr(smem + L::kOffS0);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int nq = (p.N + kTile - 1) / kTile;
+  const int qt = nq - 1 - static_cast<int>(blockIdx.x) / p.bh_q;   // heaviest (last) tiles first
+  const int bh = static_cast<int>(blockIdx.x) % p.bh_q;             // b * Hq + h
+  const int zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+  const int kv_total = nq;
+  const int n_kv = CAUSAL ? min(qt + 1, kv_total) : kv_total;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar->once_full), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(smem_addr(&bar->st_full[s]), 1);
+      mbar_init(smem_addr(&bar->st_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar->s_full), 1);
+    mbar_init(smem_addr(&bar->p_full), 4);
+    mbar_init(smem_addr(&bar->done), 1);
+    mbar_init(smem_addr(&bar->mma_final), 1);
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+  const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      const uint32_t of = smem_addr(&bar->once_full);
+      mbar_arrive_expect_tx(of, 2 * L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sQ + c * L::kChunkBytes, &tq, of, c * 64, qt * kTile, bh);
+        tma_load_3d(sDO + c * L::kChunkBytes, &tdo, of, c * 64, qt * kTile, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % L::kStages;
+        if (!mbar_wait(smem_addr(&bar->st_empty[st]), ((j / L::kStages) & 1) ^ 1, wc)) break;
+        const uint32_t f = smem_addr(&bar->st_full[st]);
+        const uint32_t dst = sSt + st * L::kStageBytes;
+        mbar_arrive_expect_tx(f, 2 * L::kTileBytes);
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_3d(dst + c * L::kChunkBytes, &tk, f, c * 64, j * kTile, zkv);
+          tma_load_3d(dst + L::kTileBytes + c * L::kChunkBytes, &tv, f, c * 64, j * kTile, zkv);
+        }
+        ++issued;
+      }
+      mbar_wait(of, 0, wc, true);
+      for (int st = 0; st < L::kStages; ++st) {
+        const int fills = issued > st ? (issued - 1 - st) / L::kStages + 1 : 0;
+        if (fills) mbar_wait(smem_addr(&bar->st_full[st]), (fills - 1) & 1, wc, true);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false);
+    constexpr uint32_t kIdescDQ = idesc_bf16_f32(kTile, D, true);
+    auto ss_group = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
+        umma_ss_warp(tmem + d_col, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    bool ok = mbar_wait_warp(smem_addr(&bar->once_full), 0, wc) &&
+              mbar_wait_warp(smem_addr(&bar->st_full[0]), 0, wc);
+    if (ok) {
+      tc_fence_after();
+      ss_group(kColS, sQ, sSt);                                  // S = Q K_0^T
+      ss_group(kColDP, sDO, sSt + L::kTileBytes);                // dP = dO V_0^T
+      umma_commit_warp(smem_addr(&bar->s_full));
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int st = j % L::kStages;
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full), j & 1, wc))) break;
+      tc_fence_after();
+      // dQ += dS K_j: A = dS (bf16 over S), B = K_j as K x N with N = d contiguous.
+      const uint32_t kb = sSt + st * L::kStageBytes;
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDQ, tmem + kColS + kk * 8, bd, kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit_warp(smem_addr(&bar->st_empty[st]));
+      if (j + 1 < n_kv) {
+        const int st1 = (j + 1) % L::kStages;
+        if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[st1]), ((j + 1) / L::kStages) & 1, wc))) break;
+        tc_fence_after();
+        const uint32_t b1 = sSt + st1 * L::kStageBytes;
+        ss_group(kColS, sQ, b1);
+        ss_group(kColDP, sDO, b1 + L::kTileBytes);
+        umma_commit_warp(smem_addr(&bar->s_full));
+      }
+    }
+    umma_commit_warp(smem_addr(&bar->done));
+    umma_commit_warp(smem_addr(&bar->mma_final));
+    __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
+  } else {
+    // -------------------------------------------------------- compute warps
+    const int row = warp * 32 + lane;             // TMEM lane = query row within the tile
+    const int qrow = qt * kTile + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const size_t vrow = static_cast<size_t>(bh) * p.n_pad + qrow;
+    const float lse2 = p.ws_lse2[vrow];
+    const float dr = p.ws_d[vrow];
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!mbar_wait_warp(smem_addr(&bar->s_full), j & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kbase = j * kTile;
+      const bool need_mask = (CAUSAL && j == qt) || (kbase + kTile > p.N);
+      // dS = P * (dP - D), P = 2^(s * scale * log2 e - lse * log2 e); masked keys get P = 0.
+      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, {
+        const int c = c2 * 2;
+        float dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = kbase + chunk * 32 + c + e;
+          const bool masked = need_mask && ((CAUSAL && key > qrow) || key >= p.N);
+          const float pv = masked ? 0.f : ex2(__uint_as_float(ra[c + e]) * sl2 - lse2);
+          dsv[e] = pv * (__uint_as_float(rb[c + e]) - dr);
+        }
+        pk[sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
+      })
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && mbar_wait_warp(smem_addr(&bar->done), 0, wc)) {
+      tc_fence_after();
+      const bool in_range = qrow < p.N;
+      __nv_bfloat16* dst = p.dq + (static_cast<size_t>(bh) * p.N + qrow) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        ATTN47_TMEM_LD32(tl + kColDQ + c0, o);
+        ATTN47_TMEM_LD_WAIT(o);
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale, __uint_as_float(o[2 * c + 1]) * p.scale);
+        if (in_range) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------- dK, dV
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                         const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
+  const uint32_t sK = smem_addr(smem + L::kOffA);
+  const uint32_t sV = smem_addr(smem + L::kOffB);
+  const uint32_t sSt = smem_addr(smem + L::kOffS0);
+  const uint32_t sVec = smem_addr(smem + L::kOffVec);
+  const float* vec = reinterpret_cast<const float*>(smem + L::kOffVec);   // [stage][lse2 | D][128]
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int nq = (p.N + kTile - 1) / kTile;
+  const int kt = static_cast<int>(blockIdx.x) / p.bh_kv;            // first key tiles see most queries
+  const int bhk = static_cast<int>(blockIdx.x) % p.bh_kv;           // b * Hkv + g
+  const int b = bhk / p.Hkv, g = bhk % p.Hkv;
+  const int qt0 = CAUSAL ? kt : 0;
+  const int per_head = nq - qt0;
+  const int steps = p.group * per_head;                              // (query head, query tile) pairs
+  auto step_q = [&](int t, int& zq, int& qt) {
+    zq = b * p.Hq + g * p.group + t / per_head;
+    qt = qt0 + t % per_head;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar->once_full), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(smem_addr(&bar->st_full[s]), 1);
+      mbar_init(smem_addr(&bar->st_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar->s_full), 1);
+    mbar_init(smem_addr(&bar->p_full), 4);
+    mbar_init(smem_addr(&bar->done), 1);
+    mbar_init(smem_addr(&bar->mma_final), 1);
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+  const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      const uint32_t of = smem_addr(&bar->once_full);
+      mbar_arrive_expect_tx(of, 2 * L::kTileBytes);
+      for (int c = 0; c < L::kChunks; ++c) {
+        tma_load_3d(sK + c * L::kChunkBytes, &tk, of, c * 64, kt * kTile, bhk);
+        tma_load_3d(sV + c * L::kChunkBytes, &tv, of, c * 64, kt * kTile, bhk);
+      }
+      int issued = 0;
+      for (int t = 0; t < steps; ++t) {
+        int zq, qt;
+        step_q(t, zq, qt);
+        const int st = t % L::kStages;
+        if (!mbar_wait(smem_addr(&bar->st_empty[st]), ((t / L::kStages) & 1) ^ 1, wc)) break;
+        const uint32_t f = smem_addr(&bar->st_full[st]);
+        const uint32_t dst = sSt + st * L::kStageBytes;
+        mbar_arrive_expect_tx(f, 2 * L::kTileBytes + 2 * kTile * 4);
+        for (int c = 0; c < L::kChunks; ++c) {
+          tma_load_3d(dst + c * L::kChunkBytes, &tq, f, c * 64, qt * kTile, zq);
+          tma_load_3d(dst + L::kTileBytes + c * L::kChunkBytes, &tdo, f, c * 64, qt * kTile, zq);
+        }
+        const size_t v0 = static_cast<size_t>(zq) * p.n_pad + static_cast<size_t>(qt) * kTile;
+        bulk_load(sVec + (st * 2 + 0) * kTile * 4, p.ws_lse2 + v0, kTile * 4, f);
+        bulk_load(sVec + (st * 2 + 1) * kTile * 4, p.ws_d + v0, kTile * 4, f);
+        ++issued;
+      }
+      mbar_wait(of, 0, wc, true);
+      for (int st = 0; st < L::kStages; ++st) {
+        const int fills = issued > st ? (issued - 1 - st) / L::kStages + 1 : 0;
+        if (fills) mbar_wait(smem_addr(&bar->st_full[st]), (fills - 1) & 1, wc, true);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false);
+    constexpr uint32_t kIdescAcc = idesc_bf16_f32(kTile, D, true);
+    auto ss_group = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
+        umma_ss_warp(tmem + d_col, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    bool ok = mbar_wait_warp(smem_addr(&bar->once_full), 0, wc);
+    for (int t = 0; t < steps && ok; ++t) {
+      const int st = t % L::kStages;
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[st]), (t / L::kStages) & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t qb = sSt + st * L::kStageBytes;
+      const uint32_t dob = qb + L::kTileBytes;
+      ss_group(kColS, sK, qb);                                   // S^T = K Q_i^T
+      ss_group(kColDP, sV, dob);                                 // dP^T = V dO_i^T
+      umma_commit_warp(smem_addr(&bar->s_full));
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full), t & 1, wc))) break;
+      tc_fence_after();
+      // dV += P^T dO_i and dK += dS^T Q_i: A from TMEM (bf16 over S^T, dP^T),
+      // B = dO_i / Q_i as K x N with N = d contiguous.
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t bdo = sdesc_sw128(dob + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDV, tmem + kColS + kk * 8, bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint64_t bq = sdesc_sw128(qb + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDK, tmem + kColDP + kk * 8, bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit_warp(smem_addr(&bar->st_empty[st]));
+    }
+    umma_commit_warp(smem_addr(&bar->done));
+    umma_commit_warp(smem_addr(&bar->mma_final));
+    __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
+  } else {
+    // -------------------------------------------------------- compute warps
+    const int row = warp * 32 + lane;             // TMEM lane = key within the tile
+    const int key = kt * kTile + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < steps; ++t) {
+      int zq, qt;
+      step_q(t, zq, qt);
+      const int st = t % L::kStages;
+      // The lse2 / D vectors of this step landed with the stage's tiles.
+      if (!mbar_wait_warp(smem_addr(&bar->st_full[st]), (t / L::kStages) & 1, wc) ||
+          !mbar_wait_warp(smem_addr(&bar->s_full), t & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float* lse2v = vec + (st * 2 + 0) * kTile;
+      const float* dv = vec + (st * 2 + 1) * kTile;
+      const int qbase = qt * kTile;
+      const bool need_mask = (CAUSAL && qt == kt) || (qbase + kTile > p.N);
+      // Row = key, column = query: P^T = 2^(s * scale * log2 e - lse2[q]),
+      // dS^T = P^T * (dP^T - D[q]); masked pairs (key > query, or a query
+      // past N) get P = 0.  P^T goes over S^T, dS^T over dP^T.
+      uint32_t dspk[2][32];
+      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, {
+        const int c = c2 * 2;
+        float pv[2];
+        float dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int qc = chunk * 32 + c + e;
+          const int q = qbase + qc;
+          const bool masked = need_mask && ((CAUSAL && key > q) || q >= p.N);
+          pv[e] = masked ? 0.f : ex2(__uint_as_float(ra[c + e]) * sl2 - lse2v[qc]);
+          dsv[e] = pv[e] * (__uint_as_float(rb[c + e]) - dv[qc]);
+        }
+        pk[sub * 16 + c2] = pack_bf16x2(pv[0], pv[1]);
+        dspk[half][sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
+      })
+      ATTN47_TMEM_ST32(tl + kColDP + 0, dspk[0]);
+      ATTN47_TMEM_ST32(tl + kColDP + 32, dspk[1]);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+    }
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && mbar_wait_warp(smem_addr(&bar->done), 0, wc)) {
+      tc_fence_after();
+      const bool in_range = key < p.N;
+      const size_t rowoff = (static_cast<size_t>(bhk) * p.N + key) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        __nv_bfloat16* dst = (which ? p.dk : p.dv) + rowoff;
+        const float mul = which ? p.scale : 1.f;
+        const uint32_t col = which ? kColDK : kColDV;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          ATTN47_TMEM_LD32(tl + col + c0, o);
+          ATTN47_TMEM_LD_WAIT(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
+          if (in_range) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) d4[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
+  using L = BwdLayout<D>;
+  const int nq = (a.N + kTile - 1) / kTile;
+  {
+    const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
+    const long long blocks = (rows + 7) / 8;
+    attn_bwd_rowdot_kernel<D><<<static_cast<unsigned>(min(blocks, 65535LL * 16)), 256, 0, a.stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  kq<<<static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_q), kThreads, L::kSmem, a.stream>>>(
+      *a.tq, *a.tk, *a.tv, *a.tdo, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
+  e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  kkv<<<static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv), kThreads, L::kSmem, a.stream>>>(
+      *a.tq, *a.tk, *a.tv, *a.tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int B, int Hq, int N) {
+  const size_t n_pad = (static_cast<size_t>(N) + kTile - 1) / kTile * kTile;
+  return 2 * static_cast<size_t>(B) * Hq * n_pad * sizeof(float);
+}
+
+int bwd_box_rows() { return kTile; }
+
+cudaError_t launch_bwd_sm103(const BwdLaunch& a) {
+  BwdParams p;
+  p.o = reinterpret_cast<const __nv_bfloat16*>(a.o);
+  p.dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
+  p.lse = a.lse;
+  p.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
+  p.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+  p.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+  p.N = a.N;
+  p.n_pad = (a.N + kTile - 1) / kTile * kTile;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.Hq / a.Hkv;
+  p.bh_q = a.B * a.Hq;
+  p.bh_kv = a.B * a.Hkv;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.ws_lse2 = a.workspace;
+  p.ws_d = a.workspace + static_cast<size_t>(p.bh_q) * p.n_pad;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  if (a.d == 128) return a.causal ? launch_t<128, true>(a, p) : launch_t<128, false>(a, p);
+  return a.causal ? launch_t<64, true>(a, p) : launch_t<64, false>(a, p);
+}
+
+}  // namespace attn47

@@ -2,7 +2,7 @@
  * attn47.h — C-ABI of the GB300 (sm_103a) exact-attention library
  * (libattn47_sm103.so).
  *
- * Two operations, both bf16 in / fp32 accumulate:
+ * Three operations, all bf16 in / fp32 accumulate:
  *
  *  attn_fwd           softmax(scale * Q K^T + causal mask) V for a whole
  *                     sequence (prefill), computed tile by tile with the
@@ -17,6 +17,10 @@
  *                     accelerate AI models", section "FlashAttention-style
  *                     attention and Paged Attention" (blocks of Q, K, V;
  *                     softmax statistics and outputs kept on chip).
+ *
+ *  attn_bwd           the gradients of attn_fwd (dQ, dK, dV), recomputing the
+ *                     attention matrix from the saved LSE ("Advanced
+ *                     attention mechanisms – II", section "Flash Attention").
  *
  *  attn_decode_paged  one query token per sequence attending to all of its
  *                     cached keys, where the KV cache is stored in fixed-size
@@ -93,6 +97,43 @@ typedef enum attn_status {
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int N, int d, int causal, float scale, void* stream);
+
+/*
+ * attn_bwd_workspace_size — bytes of device workspace attn_bwd needs: two
+ * fp32 values per query row (rows padded to multiples of 128).  0 for an
+ * empty problem.
+ */
+size_t attn_bwd_workspace_size(int B, int Hq, int N);
+
+/*
+ * attn_bwd — gradients of attn_fwd with respect to q, k and v.
+ *
+ * "Advanced attention mechanisms – II", section "Flash Attention": the
+ * forward keeps the softmax statistics (the LSE) so that the backward pass
+ * recomputes the attention matrix tile by tile instead of storing it.  With
+ * s = scale * q . k over the allowed keys and P = exp(s - lse):
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - rowsum(dO * O)),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q
+ * (for GQA, dK and dV of a KV head are summed over its query heads).
+ *
+ *  q, k, v, o    as for attn_fwd (o = its output for the same q, k, v,
+ *                causal and scale)
+ *  lse           [B, Hq, N] fp32, the LSE attn_fwd wrote for them (required)
+ *  dout          [B, Hq, N, d] bf16: dL/dO
+ *  dq            [B, Hq, N, d] bf16 (written)
+ *  dk, dv        [B, Hkv, N, d] bf16 (written)
+ *  workspace     device memory of at least attn_bwd_workspace_size(B, Hq, N)
+ *                bytes, 16-byte aligned, owned by the caller; its content on
+ *                entry does not matter and it is scratch afterwards.
+ *  Same shape rules as attn_fwd; every tensor pointer 16-byte aligned.
+ *  Errors: ATTN_ERR_INVALID_ARG (sizes, null or misaligned pointers),
+ *  ATTN_ERR_UNSUPPORTED (d), ATTN_ERR_WORKSPACE (workspace too small).
+ *  Writes only dq, dk, dv and the workspace.  Deterministic (no atomics).
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                       int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                       void* stream);
 
 /*
  * attn_decode_paged_workspace_size — bytes of device workspace that
