@@ -299,6 +299,37 @@ def fwd_config_table(attn, device, steps, peak):
     return out
 
 
+def bwd_measurement(attn, device, steps, peak):
+    """attn_bwd on the qwen_gqa_prefill workload (all three kernels per call),
+    CUDA events over `steps` calls after 3 warm-ups.  FLOPs: 2.5 x the forward
+    count (five matmuls of the forward's tile sizes against its two)."""
+    c = workloads.PREFILL_CONFIGS[FWD_CFG]
+    q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
+    g = torch.Generator().manual_seed(c["seed"] + 5)
+    do = torch.randn(q.shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    q, k, v, do = (t.to(device) for t in (q, k, v, do))
+    scale = workloads.default_scale(c["d"])
+    o, lse = attn.attn_fwd(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn.attn_bwd_workspace_size(c["B"], c["Hq"], c["N"]), dtype=torch.uint8, device=device)
+    for _ in range(3):
+        attn.attn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        attn.attn_bwd(q, k, v, o, lse, do, causal=True, scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tflops = 2.5 * fwd_flops(c) / (ms / 1e3) / 1e12
+    return {"workload": FWD_CFG + " (B4 Hq12 Hkv2 N4096 d128 causal)", "ms": ms, "tflops": tflops,
+            "frac": tflops / peak, "flop_convention": "2.5 x forward (5 matmuls vs 2)",
+            "kernels": "rowdot + dq + dkdv"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_47_gb300 as attn
 
@@ -400,6 +431,7 @@ def run_gpu(args, rank, world, local_rank):
     clock.stop()
     pk_all, _ = peaks()
     fwd_configs = fwd_config_table(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
+    backward = bwd_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
 
     # ---- max over ranks
     total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
@@ -438,6 +470,7 @@ def run_gpu(args, rank, world, local_rank):
             "fwd_configs": dict(fwd_configs, **{FWD_CFG: {
                 "shape": "B4 Hq12 Hkv2 N4096 d128 causal", "ms": fwd_sum / K,
                 "tflops": achieved_fwd, "frac": achieved_fwd / pk["bf16_tflops"]}}),
+            "backward": backward,
             "gpu_launches": 3 * K,
             "clocks": clock.summary(wall0, wall1),
         }

@@ -15,10 +15,13 @@
 //   attn_bwd_dq_kernel         one 128-row query tile per CTA, loops over K/V
 //   attn_bwd_dkdv_kernel       one 128-key tile per CTA, loops over the query
 //                              tiles of every query head of its group
-// Both tile kernels: warps 0-3 compute (one TMEM lane = one row per thread),
-// warp 4 the TMA producer, warp 5 the MMA issuer and TMEM owner.  All
-// contractions are tcgen05 MMAs with fp32 accumulators in TMEM; P and dS go
-// back into TMEM as bf16 and feed the next MMAs as their A operand.
+// Both tile kernels: warps 0-7 compute (warp w: TMEM lanes 32 (w % 4) .., one
+// row per thread, and columns 64 (w / 4) .. of the 128-wide score tiles; no
+// value crosses columns, since the LSE and D are precomputed), warp 8 the
+// TMA producer, warp 9 the MMA issuer and TMEM owner.  All contractions are
+// tcgen05 MMAs with fp32 accumulators in TMEM; P and dS go back into TMEM as
+// bf16 (each warp over the first half of its own 64 columns) and feed the
+// next MMAs as their A operand.
 #include <cuda_runtime.h>
 
 #include "bwd_sm103.h"
@@ -28,9 +31,15 @@ namespace attn47 {
 namespace {
 
 constexpr int kTile = 128;          // query rows / keys per tile (= TMEM lanes)
-constexpr int kThreads = 192;
-constexpr int kWarpLoad = 4;
-constexpr int kWarpMma = 5;
+constexpr int kThreads = 320;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+constexpr int kComputeWarps = 8;
+// TMEM column of the packed bf16 operand for K step kk (16 keys / queries):
+// keys 64h + 2c, 64h + 2c + 1 live in column 64h + c.
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -95,24 +104,22 @@ __global__ void __launch_bounds__(256) attn_bwd_rowdot_kernel(const BwdParams p)
   }
 }
 
-// Four 32-column chunks of two TMEM rows (a, b) -> callback on the fp32
-// values of each chunk; after every two chunks the callback's 32 packed bf16
-// words are stored over columns [32 * half, +32) of a, which were loaded
-// already (packed pairs fill columns half as fast as they are read).
-#define ATTN47_BWD_ROW_LOOP(TA, TB, BODY)                                                      \
-  _Pragma("unroll") for (int half = 0; half < 2; ++half) {                                     \
-    uint32_t pk[32];                                                                           \
-    _Pragma("unroll") for (int sub = 0; sub < 2; ++sub) {                                      \
-      const int chunk = half * 2 + sub;                                                        \
-      uint32_t ra[32], rb[32];                                                                 \
-      ATTN47_TMEM_LD32((TA) + chunk * 32, ra);                                                 \
-      ATTN47_TMEM_LD32((TB) + chunk * 32, rb);                                                 \
-      ATTN47_TMEM_LD_WAIT(ra);                                                                 \
-      ATTN47_TMEM_LD_WAIT(rb);                                                                 \
-      _Pragma("unroll") for (int c2 = 0; c2 < 16; ++c2) { BODY }                               \
-    }                                                                                          \
-    ATTN47_TMEM_ST32((TA) + half * 32, pk);                                                    \
-  }
+// The two 32-column chunks of this warp's 64 columns (64 h ..) of two TMEM
+// rows (a, b) -> BODY on the fp32 values of each chunk; BODY's 32 packed bf16
+// words are then stored over columns [64 h, 64 h + 32) of a, which this warp
+// has read already.
+#define ATTN47_BWD_ROW_LOOP(TA, TB, H, BODY)                                                   \
+  uint32_t pk[32];                                                                             \
+  _Pragma("unroll") for (int sub = 0; sub < 2; ++sub) {                                        \
+    const int chunk = (H) * 2 + sub;                                                           \
+    uint32_t ra[32], rb[32];                                                                   \
+    ATTN47_TMEM_LD32((TA) + chunk * 32, ra);                                                   \
+    ATTN47_TMEM_LD32((TB) + chunk * 32, rb);                                                   \
+    ATTN47_TMEM_LD_WAIT(ra);                                                                   \
+    ATTN47_TMEM_LD_WAIT(rb);                                                                   \
+    _Pragma("unroll") for (int c2 = 0; c2 < 16; ++c2) { BODY }                                 \
+  }                                                                                            \
+  ATTN47_TMEM_ST32((TA) + (H) * 64, pk);
 
 // ------------------------------------------------------------------- dQ
 template <int D, bool CAUSAL>
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bar->st_empty[s]), 1);
     }
     mbar_init(smem_addr(&bar->s_full), 1);
-    mbar_init(smem_addr(&bar->p_full), 4);
+    mbar_init(smem_addr(&bar->p_full), kComputeWarps);
     mbar_init(smem_addr(&bar->done), 1);
     mbar_init(smem_addr(&bar->mma_final), 1);
     bar->abort = 0;
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
         const uint64_t bd = sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDQ, tmem + kColS + kk * 8, bd, kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_ts_warp(tmem + kColDQ, tmem + kColS + packed_col(kk), bd, kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit_warp(smem_addr(&bar->st_empty[st]));
       if (j + 1 < n_kv) {
@@ -241,9 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
   } else {
     // -------------------------------------------------------- compute warps
-    const int row = warp * 32 + lane;             // TMEM lane = query row within the tile
+    const int quarter = warp & 3, h = warp >> 2;   // lane quarter, column half
+    const int row = quarter * 32 + lane;          // TMEM lane = query row within the tile
     const int qrow = qt * kTile + row;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const size_t vrow = static_cast<size_t>(bh) * p.n_pad + qrow;
     const float lse2 = p.ws_lse2[vrow];
     const float dr = p.ws_d[vrow];
@@ -258,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kbase = j * kTile;
       const bool need_mask = (CAUSAL && j == qt) || (kbase + kTile > p.N);
       // dS = P * (dP - D), P = 2^(s * scale * log2 e - lse * log2 e); masked keys get P = 0.
-      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, {
+      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, h, {
         const int c = c2 * 2;
         float dsv[2];
 #pragma unroll
@@ -281,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_range = qrow < p.N;
       __nv_bfloat16* dst = p.dq + (static_cast<size_t>(bh) * p.N + qrow) * D;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
         ATTN47_TMEM_LD32(tl + kColDQ + c0, o);
         ATTN47_TMEM_LD_WAIT(o);
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bar->st_empty[s]), 1);
     }
     mbar_init(smem_addr(&bar->s_full), 1);
-    mbar_init(smem_addr(&bar->p_full), 4);
+    mbar_init(smem_addr(&bar->p_full), kComputeWarps);
     mbar_init(smem_addr(&bar->done), 1);
     mbar_init(smem_addr(&bar->mma_final), 1);
     bar->abort = 0;
@@ -426,12 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
         const uint64_t bdo = sdesc_sw128(dob + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDV, tmem + kColS + kk * 8, bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_ts_warp(tmem + kColDV, tmem + kColS + packed_col(kk), bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
       }
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
         const uint64_t bq = sdesc_sw128(qb + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDK, tmem + kColDP + kk * 8, bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_ts_warp(tmem + kColDK, tmem + kColDP + packed_col(kk), bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
       }
       umma_commit_warp(smem_addr(&bar->st_empty[st]));
     }
@@ -440,9 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
   } else {
     // -------------------------------------------------------- compute warps
-    const int row = warp * 32 + lane;             // TMEM lane = key within the tile
+    const int quarter = warp & 3, h = warp >> 2;   // lane quarter, column half
+    const int row = quarter * 32 + lane;          // TMEM lane = key within the tile
     const int key = kt * kTile + row;
-    const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < steps; ++t) {
@@ -463,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Row = key, column = query: P^T = 2^(s * scale * log2 e - lse2[q]),
       // dS^T = P^T * (dP^T - D[q]); masked pairs (key > query, or a query
       // past N) get P = 0.  P^T goes over S^T, dS^T over dP^T.
-      uint32_t dspk[2][32];
-      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, {
+      uint32_t dspk[32];
+      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, h, {
         const int c = c2 * 2;
         float pv[2];
         float dsv[2];
@@ -477,10 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           dsv[e] = pv[e] * (__uint_as_float(rb[c + e]) - dv[qc]);
         }
         pk[sub * 16 + c2] = pack_bf16x2(pv[0], pv[1]);
-        dspk[half][sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
+        dspk[sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
       })
-      ATTN47_TMEM_ST32(tl + kColDP + 0, dspk[0]);
-      ATTN47_TMEM_ST32(tl + kColDP + 32, dspk[1]);
+      ATTN47_TMEM_ST32(tl + kColDP + h * 64, dspk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -497,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mul = which ? p.scale : 1.f;
         const uint32_t col = which ? kColDK : kColDV;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
           uint32_t o[32];
           ATTN47_TMEM_LD32(tl + col + c0, o);
           ATTN47_TMEM_LD_WAIT(o);
