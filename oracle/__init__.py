@@ -12,9 +12,12 @@ Sources (web pages, cited by title and section):
   * "Fast attention kernels and operator fusion accelerate AI models":
     section "FlashAttention-style attention and Paged Attention".
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against brute
-force, closed forms, a library routine and invariants the mathematics fixes.
-No function is "parity unpinned".
+Every function here is pinned against brute force, closed forms, a library
+routine and invariants the mathematics fixes: the forward and decode by
+``tests/test_oracle_pins.py``, the backward by
+``tests/test_oracle_backward_pins.py``, the chunked prefill over a paged
+cache by ``tests/test_oracle_paged_prefill_pins.py``.  No function is
+"parity unpinned".
 """
 
 from .definitions import (  # noqa: F401
@@ -24,6 +27,7 @@ from .definitions import (  # noqa: F401
     combine_partials,
     decode_paged,
     gather_paged_keys,
+    prefill_paged,
     score_matrix,
     softmax_probs,
     split_partials,

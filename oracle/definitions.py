@@ -1,4 +1,5 @@
-"""fp64 reference definitions of exact attention (prefill and paged decode).
+"""fp64 reference definitions of exact attention (prefill, paged decode,
+chunked prefill over a paged cache, and the backward pass).
 
 TEST INFRASTRUCTURE ONLY — see the package docstring.  Nothing on the GPU
 product path imports this module.
@@ -11,6 +12,9 @@ Layouts (the pages fix none; these are the readings used everywhere):
   decode   q [S, Hq, d]; k_cache/v_cache [num_blocks, Hkv, block_size, d];
            block_table [S, max_blocks] int; seq_lens [S] int;
            o [S, Hq, d]; lse [S, Hq]
+  chunked  q [S, Hq, N, d] new queries, k_new/v_new [S, Hkv, N, d];
+  prefill  paged caches and block_table as for decode; ctx_lens [S] int
+           (tokens already cached); o [S, Hq, N, d]; lse [S, Hq, N]
 Query head h reads KV head g = h // (Hq // Hkv) (contiguous GQA groups).
 LSE is the natural log of the sum of exp of the *scaled* logits.
 """
@@ -295,3 +299,67 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale,
             o[b, heads] = p @ vv
             lse[b, heads] = m + np.log(l)
     return o, lse
+
+
+def prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scale,
+                  block_size=16):
+    """Chunked prefill over a paged KV cache (plain definition).
+
+    "Fast attention kernels and operator fusion accelerate AI models",
+    section "FlashAttention-style attention and Paged Attention": the KV cache
+    grows as tokens arrive and lives in fixed-size blocks that a block table
+    maps from logical positions; every position goes through that table.
+    The step that fills the cache for a chunk of new tokens is read as:
+
+      1. append: new token i of sequence b takes logical position
+         ctx_lens[b] + i; its key and value rows are stored at
+         cache[block_table[b][pos // block_size], g, pos % block_size];
+      2. the slots past the sequence's new length in its last block are set
+         to zero (they hold no token; clearing them keeps stale values out of
+         the block);
+      3. attend: new query i (position ctx_lens[b] + i) sees logical keys
+         0 .. ctx_lens[b] + i — the whole cached prefix plus the new tokens up
+         to itself (the causal mask at an offset) — gathered through the
+         table (``gather_paged_keys``), with the definition of ``attention``.
+
+    q [S, Hq, N, d]; k_new / v_new [S, Hkv, N, d]; caches
+    [num_blocks, Hkv, block_size, d] (not modified: updated copies are
+    returned); block_table [S, max_blocks] int; ctx_lens [S] int.
+    Returns (o [S, Hq, N, d], lse [S, Hq, N], k_cache_out, v_cache_out), fp64.
+    """
+    q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    S, Hq, N, d = q.shape
+    Hkv = k_new.shape[1]
+    group = Hq // Hkv
+    # Steps 1 and 2: the cache update.
+    for b in range(S):
+        ctx = int(ctx_lens[b])
+        for g in range(Hkv):
+            for i in range(N):
+                pos = ctx + i
+                phys = int(block_table[b][pos // block_size])
+                kc[phys, g, pos % block_size] = k_new[b, g, i]
+                vc[phys, g, pos % block_size] = v_new[b, g, i]
+            end = ctx + N
+            if N > 0 and end % block_size != 0:
+                phys = int(block_table[b][end // block_size])
+                kc[phys, g, end % block_size:] = 0.0
+                vc[phys, g, end % block_size:] = 0.0
+    # Step 3: attention of the new queries over the updated cache.
+    o = np.zeros((S, Hq, N, v_new.shape[3]))
+    lse = np.zeros((S, Hq, N))
+    for b in range(S):
+        ctx = int(ctx_lens[b])
+        n_keys = ctx + N
+        allowed = np.arange(n_keys)[None, :] <= (ctx + np.arange(N))[:, None]
+        for g in range(Hkv):
+            kk = gather_paged_keys(kc, block_table[b], n_keys, g, block_size)
+            vv = gather_paged_keys(vc, block_table[b], n_keys, g, block_size)
+            for h in range(g * group, (g + 1) * group):
+                s = score_matrix(q[b, h], kk, scale)
+                p, m, l = softmax_probs(s, allowed)
+                o[b, h] = p @ vv
+                lse[b, h] = m + np.log(l)
+    return o, lse, kc, vc

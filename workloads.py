@@ -107,3 +107,73 @@ def decode_inputs(num_seqs, Hq, Hkv, d, seed, len_lo=128, len_hi=4096,
     return dict(q=q, k_cache=k_cache, v_cache=v_cache, block_table=table,
                 seq_lens=seq_lens.to(torch.int32), block_size=block_size,
                 max_blocks_per_seq=max_blocks_per_seq, num_blocks=num_blocks)
+
+
+PAGED_PREFILL_CONFIGS = {
+    # A chunk of 2048 new tokens per sequence on top of a cached prefix, with
+    # the Qwen2.5-1.5B-style GQA geometry and block_size = 16.
+    "qwen_chunked_prefill": dict(num_seqs=4, Hq=12, Hkv=2, N_new=2048, d=128,
+                                 ctx_lo=0, ctx_hi=6144, seed=5),
+}
+
+
+def paged_prefill_inputs(num_seqs, Hq, Hkv, N_new, d, seed, ctx_lo=0, ctx_hi=4096,
+                         ctx_lens=None, block_size=BLOCK_SIZE, permute=True,
+                         nan_unused=True, max_blocks_per_seq=None, spare_blocks=0):
+    """Chunked-prefill inputs over a paged cache.
+
+    Sequence b already holds ctx_lens[b] ~ U{ctx_lo..ctx_hi} cached tokens
+    (unless given) and brings N_new new ones.  Its table row gets
+    ceil((ctx + N_new) / 16) blocks: a consecutive slice of one random
+    permutation of the pool (identity when ``permute`` is False), padded
+    with -1.  The prefix keys/values are drawn in logical order and stored
+    through the table; every other slot of the pool (the slots the new
+    tokens will take, the tail of each last block, ``spare_blocks``) holds
+    NaN when ``nan_unused``, else N(0, 1) draws.
+
+    Returns a dict of CPU tensors: q [S,Hq,N_new,d], k_new / v_new
+    [S,Hkv,N_new,d], k_cache / v_cache [num_blocks,Hkv,block_size,d] bf16,
+    block_table [S,max_blocks] int32, ctx_lens [S] int32, and k_prefix /
+    v_prefix (lists of [Hkv, ctx_lens[b], d] bf16: the same prefix values in
+    logical order), plus block_size, max_blocks_per_seq, num_blocks.
+    """
+    gen = torch.Generator().manual_seed(int(seed))
+    if ctx_lens is None:
+        ctx_lens = torch.randint(ctx_lo, ctx_hi + 1, (num_seqs,), generator=gen)
+    ctx_lens = torch.as_tensor(ctx_lens, dtype=torch.int64)
+    total = [int(c) + int(N_new) for c in ctx_lens]
+    nblk = [(t + block_size - 1) // block_size for t in total]
+    if max_blocks_per_seq is None:
+        max_blocks_per_seq = max(nblk + [1])
+    num_blocks = max(sum(nblk) + int(spare_blocks), 1)
+    perm = torch.randperm(num_blocks, generator=gen) if permute else torch.arange(num_blocks)
+    table = torch.full((num_seqs, max_blocks_per_seq), -1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    q = _randn(gen, (num_seqs, Hq, N_new, d)).to(torch.bfloat16)
+    k_new = _randn(gen, (num_seqs, Hkv, N_new, d)).to(torch.bfloat16)
+    v_new = _randn(gen, (num_seqs, Hkv, N_new, d)).to(torch.bfloat16)
+    shape = (num_blocks, Hkv, block_size, d)
+    if nan_unused:
+        k_cache = torch.full(shape, float("nan"), dtype=torch.bfloat16)
+        v_cache = torch.full(shape, float("nan"), dtype=torch.bfloat16)
+    else:
+        k_cache = _randn(gen, shape).to(torch.bfloat16)
+        v_cache = _randn(gen, shape).to(torch.bfloat16)
+    k_prefix, v_prefix = [], []
+    for b, c in enumerate(ctx_lens.tolist()):
+        kp = _randn(gen, (Hkv, c, d)).to(torch.bfloat16)
+        vp = _randn(gen, (Hkv, c, d)).to(torch.bfloat16)
+        pos = torch.arange(c)
+        phys = table[b, pos // block_size].long()
+        slot = pos % block_size
+        k_cache[phys, :, slot] = kp.permute(1, 0, 2)
+        v_cache[phys, :, slot] = vp.permute(1, 0, 2)
+        k_prefix.append(kp)
+        v_prefix.append(vp)
+    return dict(q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                block_table=table, ctx_lens=ctx_lens.to(torch.int32), k_prefix=k_prefix,
+                v_prefix=v_prefix, block_size=block_size,
+                max_blocks_per_seq=max_blocks_per_seq, num_blocks=num_blocks)
