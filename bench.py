@@ -330,6 +330,57 @@ def bwd_measurement(attn, device, steps, peak):
             "kernels": "rowdot + dq + dkdv"}
 
 
+def paged_prefill_flops(ctx_lens, Hq, N, d):
+    """Causal pairs of a chunk: new query i sees ctx + i + 1 keys."""
+    pairs = sum(N * int(c) + N * (N + 1) // 2 for c in ctx_lens)
+    return 4.0 * d * Hq * pairs
+
+
+def paged_prefill_measurement(attn, device, steps, peak):
+    """attn_prefill_paged on the chunked-prefill workload (2048 new tokens on
+    top of a cached prefix of U[0, 6144] tokens, 4 sequences, Qwen-style GQA,
+    block_size 16, permuted table): the append and the attention kernel per
+    call, CUDA events over `steps` calls after 3 warm-ups, three input sets
+    (about 60 MB each) in rotation so they exceed L2.  Appending the same rows
+    at the same positions again leaves the cache as it was, so every call does
+    the same work."""
+    c = workloads.PAGED_PREFILL_CONFIGS["qwen_chunked_prefill"]
+    sets, flops = [], []
+    for i in range(3):
+        x = workloads.paged_prefill_inputs(c["num_seqs"], c["Hq"], c["Hkv"], c["N_new"], c["d"],
+                                           c["seed"] + 100 * i, ctx_lo=c["ctx_lo"], ctx_hi=c["ctx_hi"])
+        flops.append(paged_prefill_flops(x["ctx_lens"].tolist(), c["Hq"], c["N_new"], c["d"]))
+        d = {n: x[n].to(device) for n in ("q", "k_new", "v_new", "k_cache", "v_cache",
+                                          "block_table", "ctx_lens")}
+        d["o"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=device)
+        sets.append(d)
+    scale = workloads.default_scale(c["d"])
+
+    def call(d):
+        attn.attn_prefill_paged(d["q"], d["k_new"], d["v_new"], d["k_cache"], d["v_cache"],
+                                d["block_table"], d["ctx_lens"], scale=scale, o=d["o"], lse=d["lse"])
+
+    for i in range(3):
+        call(sets[i % 3])
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        call(sets[i % 3])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    mean_flops = sum(flops[i % 3] for i in range(steps)) / steps
+    tflops = mean_flops / (ms / 1e3) / 1e12
+    return {"workload": "qwen_chunked_prefill (4 seqs, N_new 2048, ctx~U[0,6144], Hq12 Hkv2 d128, "
+                        "block_size 16)", "ms": ms, "tflops": tflops, "frac": tflops / peak,
+            "flop_convention": "4*d*Hq*sum_b(N*ctx_b + N(N+1)/2) (causal pairs)",
+            "kernels": "kv append + attention (paged mode)", "gpu_launches_per_call": 2}
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_47_gb300 as attn
 
@@ -432,6 +483,7 @@ def run_gpu(args, rank, world, local_rank):
     pk_all, _ = peaks()
     fwd_configs = fwd_config_table(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
     backward = bwd_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
+    paged_prefill = paged_prefill_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
 
     # ---- max over ranks
     total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
@@ -471,6 +523,7 @@ def run_gpu(args, rank, world, local_rank):
                 "shape": "B4 Hq12 Hkv2 N4096 d128 causal", "ms": fwd_sum / K,
                 "tflops": achieved_fwd, "frac": achieved_fwd / pk["bf16_tflops"]}}),
             "backward": backward,
+            "paged_prefill": paged_prefill,
             "gpu_launches": 3 * K,
             "clocks": clock.summary(wall0, wall1),
         }

@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) exact attention: tiled online-softmax prefill and paged-KV decode.
+"""GB300 (sm_103a) exact attention: tiled online-softmax prefill, its backward,
+paged-KV decode and chunked prefill over the paged cache.
 
 The compute lives in ``lib/libattn47_sm103.so`` (hand-written CUDA, C-ABI
 declared in ``include/attn47.h``); this package is its Python binding.
@@ -19,6 +20,7 @@ from ._binding import (  # noqa: F401
     attn_decode_paged_noalloc,
     attn_decode_paged_workspace_size,
     attn_fwd,
+    attn_prefill_paged,
     device_status,
     library_path,
     load_library,

@@ -34,6 +34,8 @@ _SIGS = {
                                _P, _P, _P, ctypes.c_size_t, _P]),
     "attn_decode_paged_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                                        _P, _P, _P]),
+    "attn_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                ctypes.c_float, _P, _P, _P]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
@@ -260,6 +262,54 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=
                                        block_table.shape[1], num_blocks, float(scale), _ptr(o),
                                        _ptr(lse), _stream_handle(stream))
     _check("attn_decode_paged_noalloc", st)
+    return o, lse
+
+
+def attn_prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scale=None,
+                       o=None, lse=None, return_lse=True, stream=None):
+    """Chunked prefill over a paged cache (all tensors on the GPU).
+
+    q [S,Hq,N,d], k_new / v_new [S,Hkv,N,d] bf16; caches
+    [num_blocks,Hkv,16,d] bf16 (updated in place: the new rows are appended at
+    positions ctx_lens[b] + i); block_table [S,max_blocks] int32; ctx_lens [S]
+    int32 (left unchanged).  Returns (o [S,Hq,N,d] bf16, lse [S,Hq,N] fp32 or
+    None).
+    """
+    lib = load_library()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k_new", k_new, torch.bfloat16),
+                        ("v_new", v_new, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
+                        ("v_cache", v_cache, torch.bfloat16), ("block_table", block_table, torch.int32),
+                        ("ctx_lens", ctx_lens, torch.int32)):
+        _need_cuda(name, t, dt)
+    if q.dim() != 4 or k_new.dim() != 4 or k_new.shape != v_new.shape:
+        raise ValueError("q must be [S,Hq,N,d] and k_new / v_new [S,Hkv,N,d]")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("caches must be [num_blocks,Hkv,block_size,d]")
+    S, Hq, N, d = q.shape
+    num_blocks, Hkv, block_size, dc = k_cache.shape
+    if k_new.shape != (S, Hkv, N, d) or dc != d:
+        raise ValueError("k_new / v_new must be [S, Hkv, N, d] matching q and the caches")
+    if block_table.dim() != 2 or block_table.shape[0] != S or tuple(ctx_lens.shape) != (S,):
+        raise ValueError("block_table must be [S, max_blocks] and ctx_lens [S]")
+    if scale is None:
+        scale = d ** -0.5
+    if o is None:
+        o = torch.empty_like(q)
+    else:
+        _need_cuda("o", o, torch.bfloat16)
+        if o.shape != q.shape:
+            raise ValueError("o must have q's shape")
+    if lse is None and return_lse:
+        lse = torch.empty((S, Hq, N), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _need_cuda("lse", lse, torch.float32)
+        if tuple(lse.shape) != (S, Hq, N):
+            raise ValueError("lse must be [S, Hq, N]")
+    st = lib.attn_prefill_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_table), _ptr(ctx_lens), S, Hq, Hkv, N, d, block_size,
+                                block_table.shape[1], num_blocks, float(scale), _ptr(o), _ptr(lse),
+                                _stream_handle(stream))
+    _check("attn_prefill_paged", st)
     return o, lse
 
 

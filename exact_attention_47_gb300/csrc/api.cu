@@ -403,6 +403,100 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
                            kNoAllocScratchBytes, stream);
 }
 
+attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, const int32_t* block_table,
+                                 const int32_t* ctx_lens, int num_seqs, int Hq, int Hkv, int N,
+                                 int d, int block_size, int max_blocks_per_seq, int num_blocks,
+                                 float scale, void* o, float* lse, void* stream) {
+  if (num_seqs < 0 || N < 0 || Hq < 1 || Hkv < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy num_seqs >= 0, N >= 0, Hq, Hkv, "
+                "max_blocks_per_seq, num_blocks >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (block_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size < N)
+    return fail(ATTN_ERR_INVALID_ARG, "N (%d) new tokens do not fit in max_blocks_per_seq (%d) blocks",
+                N, max_blocks_per_seq);
+  if (num_seqs == 0 || N == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_table || !ctx_lens || !o)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k_new, v_new, caches, block_table, ctx_lens and o must be non-null");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "q, k_new, v_new, caches and o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(ctx_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "block_table, ctx_lens and lse must be 4-byte aligned");
+  const long long tiles = (static_cast<long long>(N) + 127) / 128;
+  if (static_cast<long long>(num_seqs) * Hq * tiles > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+
+  const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(attn47::fwd_box_rows()), 1};
+  const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                               static_cast<cuuint64_t>(num_seqs) * Hq};
+  // The cache as [num_blocks][Hkv][16][d]: one box is the 16 slots of one
+  // (block, KV head), 64 columns wide.
+  const cuuint32_t cbox[4] = {64, 16, 1, 1};
+  const cuuint64_t cdims[4] = {static_cast<cuuint64_t>(d), 16, static_cast<cuuint64_t>(Hkv),
+                               static_cast<cuuint64_t>(num_blocks)};
+  alignas(64) CUtensorMap tq, tk, tv;
+  if ((st = encode_bf16(&tq, q, 3, qdims, qbox)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tk, k_cache, 4, cdims, cbox)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tv, v_cache, 4, cdims, cbox)) != ATTN_OK) return st;
+
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn47::AppendLaunch w;
+  w.k_new = k_new;
+  w.v_new = v_new;
+  w.k_cache = k_cache;
+  w.v_cache = v_cache;
+  w.block_table = block_table;
+  w.ctx_lens = ctx_lens;
+  w.B = num_seqs;
+  w.Hkv = Hkv;
+  w.N = N;
+  w.d = d;
+  w.max_blocks = max_blocks_per_seq;
+  w.num_blocks = num_blocks;
+  w.sms = dev->sms;
+  w.status = dev->status;
+  w.stream = s;
+  st = launch_result(attn47::launch_kv_append_sm103(w), "attn_prefill_paged (append)");
+  if (st != ATTN_OK) return st;
+
+  attn47::FwdLaunch a;
+  a.tq = &tq;
+  a.tk = &tk;
+  a.tv = &tv;
+  a.o = o;
+  a.lse = lse;
+  a.B = num_seqs;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.d = d;
+  a.causal = true;
+  a.scale = scale;
+  a.sms = dev->sms;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = s;
+  a.paged = true;
+  a.block_table = block_table;
+  a.ctx_lens = ctx_lens;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  return launch_result(attn47::launch_fwd_sm103(a), "attn_prefill_paged (attention)");
+}
+
 attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {
   if (!flags_out) return fail(ATTN_ERR_INVALID_ARG, "flags_out must be non-null");
   DeviceInfo* dev = nullptr;

@@ -32,6 +32,18 @@
 // tile maximum exceeds it by more than 2^8 (in the exp2 domain), so O and l
 // are rescaled rarely; exponents stay <= 8, numerators <= 256, and the final
 // O / l and LSE are the same function of the same stabiliser.
+//
+// Paged mode (chunked prefill over a paged KV cache; same page, same
+// section: the cache lives in fixed-size blocks and every position goes
+// through the block table): the N query rows of sequence b are its new
+// tokens at positions ctx_b .. ctx_b + N - 1, and K/V come from the cache.
+// A 128-key tile is eight 16-slot blocks; the producer looks each one up in
+// the table and loads it as its own 16-row TMA box into the same swizzled
+// tile (the 128-byte swizzle repeats every 8 rows, so eight 16-row boxes at
+// 2 KB steps land exactly where one 128-row box would).  Blocks past the
+// sequence use a block index outside the pool, which the TMA unit fills
+// with zeros.  Query row i may see keys 0 .. ctx_b + i: the causal mask at an
+// offset, so it can fall across two key tiles.
 #include <cuda_runtime.h>
 
 #include "fwd_sm103.h"
@@ -91,9 +103,17 @@ struct FwdParams {
   float scale_log2;
   unsigned int* status;
   unsigned long long timeout_ns;
+  // paged mode only
+  const int* block_table;   // [B, max_blocks]
+  const int* ctx_lens;      // [B] tokens cached before the N new ones
+  int max_blocks, num_blocks;
+  int max_ctx;              // max_blocks * 16 - N: largest valid ctx_lens entry
 };
 
-template <int D, bool CAUSAL>
+constexpr int kPageRows = 16;                        // token slots per cache block
+constexpr int kPagesPerTile = kBN / kPageRows;
+
+template <int D, bool CAUSAL, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk,
@@ -122,16 +142,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_total = (p.N + kBN - 1) / kBN;
   struct Unit {
     int qblk, zq, zkv, nA, nB;
+    int pos0, b, kvh, nblk;                            // paged: ctx_b, sequence, KV head, blocks
   };
   auto unit_info = [&](int k) {
     Unit u;
     u.qblk = p.num_q_blocks - 1 - k / p.bh_total;
     const int bh = k % p.bh_total;
     u.zq = bh;                                         // b * Hq + h
-    u.zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
-    // K/V tiles each query tile needs; the diagonal tile of tile X is 2*qblk + X.
-    u.nA = CAUSAL ? min(2 * u.qblk + 1, kv_total) : kv_total;
-    u.nB = CAUSAL ? min(2 * u.qblk + 2, kv_total) : kv_total;
+    u.b = bh / p.Hq;
+    u.kvh = (bh % p.Hq) / p.group;
+    u.zkv = u.b * p.Hkv + u.kvh;
+    if constexpr (PAGED) {
+      // A ctx_lens entry outside [0, max_ctx] was reported by the append
+      // kernel; it is clamped here so every loop stays bounded.
+      u.pos0 = min(max(__ldg(p.ctx_lens + u.b), 0), p.max_ctx);
+      const int lastA = min(u.qblk * kRowsPerCta + kBM - 1, p.N - 1);
+      const int lastB = min(u.qblk * kRowsPerCta + 2 * kBM - 1, p.N - 1);
+      u.nA = (u.pos0 + lastA) / kBN + 1;               // tiles up to key pos0 + last row
+      u.nB = (u.pos0 + lastB) / kBN + 1;
+      u.nblk = min((u.pos0 + p.N + kPageRows - 1) / kPageRows, p.max_blocks);
+    } else {
+      u.pos0 = 0;
+      u.nblk = 0;
+      // K/V tiles each query tile needs; the diagonal tile of tile X is 2*qblk + X.
+      u.nA = CAUSAL ? min(2 * u.qblk + 1, kv_total) : kv_total;
+      u.nB = CAUSAL ? min(2 * u.qblk + 2, kv_total) : kv_total;
+    }
     return u;
   };
 
@@ -197,21 +233,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int g = kv_issued + j;
           const int st = g % L::kStages;
           const uint32_t ph = (g / L::kStages) & 1;
+          // Paged: the physical blocks of this tile (read before the wait, so
+          // the table lookups overlap it); p.num_blocks lies outside the pool.
+          int page[PAGED ? kPagesPerTile : 1];
+          if constexpr (PAGED) {
+            const int* row = p.block_table + static_cast<size_t>(u.b) * p.max_blocks;
+#pragma unroll
+            for (int i = 0; i < kPagesPerTile; ++i) {
+              const int lb = j * kPagesPerTile + i;
+              page[i] = lb < u.nblk ? __ldg(row + lb) : p.num_blocks;
+            }
+#pragma unroll
+            for (int i = 0; i < kPagesPerTile; ++i) {
+              // An entry outside the pool is reported and read as zeros.
+              if (j * kPagesPerTile + i < u.nblk &&
+                  static_cast<unsigned>(page[i]) >= static_cast<unsigned>(p.num_blocks)) {
+                atomicOr(p.status, kDevBadBlock);
+                page[i] = p.num_blocks;
+              }
+            }
+          }
+          auto load_kv = [&](uint32_t dst, const CUtensorMap* map, uint32_t full) {
+            mbar_arrive_expect_tx(full, L::kKV);
+            if constexpr (PAGED) {
+#pragma unroll
+              for (int i = 0; i < kPagesPerTile; ++i)
+                for (int c = 0; c < L::kChunks; ++c)
+                  tma_load_4d(dst + c * L::kKVChunk + i * kPageRows * 128, map, full, c * 64, 0, u.kvh,
+                              page[i]);
+            } else {
+              for (int c = 0; c < L::kChunks; ++c)
+                tma_load_3d(dst + c * L::kKVChunk, map, full, c * 64, j * kBN, u.zkv);
+            }
+          };
           if (!(ok = mbar_wait(smem_addr(&bar->k_empty[st]), ph ^ 1, wc))) break;
-          const uint32_t kf = smem_addr(&bar->k_full[st]);
-          mbar_arrive_expect_tx(kf, L::kKV);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sK + st * L::kKV + c * L::kKVChunk, &tk, kf, c * 64, j * kBN, u.zkv);
+          load_kv(sK + st * L::kKV, &tk, smem_addr(&bar->k_full[st]));
           ++k_issued;
           if (j == 0) {
             load_q(1);
             if (!ok) break;
           }
           if (!(ok = mbar_wait(smem_addr(&bar->v_empty[st]), ph ^ 1, wc))) break;
-          const uint32_t vf = smem_addr(&bar->v_full[st]);
-          mbar_arrive_expect_tx(vf, L::kKV);
-          for (int c = 0; c < L::kChunks; ++c)
-            tma_load_3d(sV + st * L::kKV + c * L::kKVChunk, &tv, vf, c * 64, j * kBN, u.zkv);
+          load_kv(sV + st * L::kKV, &tv, smem_addr(&bar->v_full[st]));
           ++v_issued;
         }
         kv_issued += u.nB;
@@ -408,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qrow = u.qblk * kRowsPerCta + x * kBM + row;
     const int n_kv = x ? u.nB : u.nA;
     const int diag = 2 * u.qblk + x;               // causal: the tile holding key == row
+    const int qpos = u.pos0 + qrow;                // paged: position of this row's token
+    const int qpos_first = u.pos0 + u.qblk * kRowsPerCta + x * kBM;
     const int zq = u.zq;
     float m = 0.f;                                 // stabiliser in use (exp2 domain)
     float l = 0.f;                                 // denominator relative to m (fp32 terms)
@@ -438,12 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         s[96 + c] = __uint_as_float(r3[c]);
       }
       const int kbase = j * kBN;
-      const bool need_mask = CAUSAL ? (j == diag) : (kbase + kBN > p.N);
+      const bool need_mask = PAGED ? (kbase + kBN - 1 > qpos_first)
+                                   : CAUSAL ? (j == diag) : (kbase + kBN > p.N);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
           const int key = kbase + c;
-          const bool masked = CAUSAL ? (key > qrow) : (key >= p.N);
+          const bool masked = PAGED ? (key > qpos) : CAUSAL ? (key > qrow) : (key >= p.N);
           s[c] = masked ? -INFINITY : s[c];
         }
       }
@@ -570,10 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAGED>
 cudaError_t launch_t(const FwdLaunch& a) {
   using L = FwdLayout<D>;
-  auto kern = attn_fwd_sm103_kernel<D, CAUSAL>;
+  auto kern = attn_fwd_sm103_kernel<D, CAUSAL, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -589,6 +655,11 @@ cudaError_t launch_t(const FwdLaunch& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.block_table = a.block_table;
+  p.ctx_lens = a.ctx_lens;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.max_ctx = PAGED ? a.max_blocks * kPageRows - a.N : 0;
   // Persistent: one CTA per SM (shared memory allows one), each walking units.
   const unsigned grid = static_cast<unsigned>(min(p.num_units, a.sms > 0 ? a.sms : 1));
   kern<<<grid, kThreads, L::kSmem, a.stream>>>(*a.tq, *a.tk, *a.tv, p);
@@ -600,8 +671,9 @@ cudaError_t launch_t(const FwdLaunch& a) {
 int fwd_box_rows() { return kBM; }
 
 cudaError_t launch_fwd_sm103(const FwdLaunch& a) {
-  if (a.d == 128) return a.causal ? launch_t<128, true>(a) : launch_t<128, false>(a);
-  return a.causal ? launch_t<64, true>(a) : launch_t<64, false>(a);
+  if (a.paged) return a.d == 128 ? launch_t<128, true, true>(a) : launch_t<64, true, true>(a);
+  if (a.d == 128) return a.causal ? launch_t<128, true, false>(a) : launch_t<128, false, false>(a);
+  return a.causal ? launch_t<64, true, false>(a) : launch_t<64, false, false>(a);
 }
 
 }  // namespace attn47

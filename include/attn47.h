@@ -2,7 +2,7 @@
  * attn47.h — C-ABI of the GB300 (sm_103a) exact-attention library
  * (libattn47_sm103.so).
  *
- * Three operations, all bf16 in / fp32 accumulate:
+ * Four operations, all bf16 in / fp32 accumulate:
  *
  *  attn_fwd           softmax(scale * Q K^T + causal mask) V for a whole
  *                     sequence (prefill), computed tile by tile with the
@@ -30,6 +30,13 @@
  *                     models", section "FlashAttention-style attention and
  *                     Paged Attention" (paged cache, block table, per-position
  *                     translation; block_size = 16 in its worked example).
+ *
+ *  attn_prefill_paged a chunk of new tokens per sequence: their keys and
+ *                     values are appended to the same paged cache, then each
+ *                     new query attends causally to the cached prefix and the
+ *                     new tokens up to itself (same page and section: the
+ *                     cache grows as tokens arrive; the serving example runs
+ *                     prefill, then decode, over block_size = 16 blocks).
  *
  * Conventions shared by every call
  *  - Pointers are DEVICE pointers of the current CUDA device unless stated.
@@ -63,7 +70,7 @@
 extern "C" {
 #endif
 
-#define ATTN47_ABI_VERSION 1
+#define ATTN47_ABI_VERSION 2
 
 typedef enum attn_status {
   ATTN_OK = 0,
@@ -79,8 +86,10 @@ typedef enum attn_status {
 #define ATTN_DEV_TIMEOUT 0x1u    /* a kernel wait exceeded its time limit; outputs invalid */
 #define ATTN_DEV_BAD_BLOCK 0x2u  /* a block-table entry was outside [0, num_blocks); that block
                                     was skipped */
-#define ATTN_DEV_BAD_SEQLEN 0x4u /* a seq_lens entry was < 0 or > max_blocks_per_seq*block_size;
-                                    it was clamped into range */
+#define ATTN_DEV_BAD_SEQLEN 0x4u /* a seq_lens entry was < 0 or > max_blocks_per_seq*block_size
+                                    (decode), or a ctx_lens entry was < 0 or
+                                    > max_blocks_per_seq*block_size - N (chunked prefill);
+                                    it was clamped into range, outputs of that sequence invalid */
 
 /*
  * attn_fwd — exact attention forward (prefill).
@@ -205,6 +214,47 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
                                         int num_seqs, int Hq, int Hkv, int d, int block_size,
                                         int max_blocks_per_seq, int num_blocks, float scale,
                                         void* o, float* lse, void* stream);
+
+/*
+ * attn_prefill_paged — chunked prefill over a paged KV cache.
+ *
+ * "Fast attention kernels and operator fusion accelerate AI models",
+ * section "FlashAttention-style attention and Paged Attention": the KV cache
+ * grows token by token in fixed-size blocks, a block table maps logical
+ * positions to physical blocks, and the attention kernel translates every
+ * position through it.  For each sequence b, with P = ctx_lens[b] tokens
+ * already cached:
+ *   1. new token i (0 <= i < N) is stored at logical position P + i, i.e.
+ *      slot (P + i) % 16 of physical block block_table[b][(P + i) / 16], for
+ *      every KV head; the slots past P + N in the last block are set to 0;
+ *   2. new query i attends to logical keys 0 .. P + i (the cached prefix and
+ *      the new tokens up to itself) — softmax(scale * q . k) v over them.
+ *
+ *  q            [num_seqs, Hq, N, d] bf16: the new tokens' queries
+ *  k_new, v_new [num_seqs, Hkv, N, d] bf16: their keys and values
+ *  k_cache,
+ *  v_cache      [num_blocks, Hkv, block_size, d] bf16 (read and written)
+ *  block_table  [num_seqs, max_blocks_per_seq] int32 (device): must map the
+ *               ceil((P + N) / 16) blocks of each sequence; blocks are owned by
+ *               one sequence (two sequences writing the same block race)
+ *  ctx_lens     [num_seqs] int32 (device): P of each sequence, 0 <= P <=
+ *               max_blocks_per_seq * 16 - N; not modified (after the call the
+ *               sequence holds P + N tokens)
+ *  o            [num_seqs, Hq, N, d] bf16 (written)
+ *  lse          [num_seqs, Hq, N] fp32 (written) or NULL
+ *  block_size must be 16; d must be 64 or 128; Hq % Hkv == 0;
+ *  N <= max_blocks_per_seq * 16.  All bf16 tensors 16-byte aligned.
+ *  num_seqs == 0 or N == 0 is an empty problem: ATTN_OK, nothing launched.
+ *  Launches two kernels in stream order: the append, then the attention.
+ *  Table entries outside [0, num_blocks) set ATTN_DEV_BAD_BLOCK (the append
+ *  skips them; the attention reads that block as zeros); invalid ctx_lens
+ *  set ATTN_DEV_BAD_SEQLEN.  Deterministic (no atomics on data).
+ */
+attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, const int32_t* block_table,
+                                 const int32_t* ctx_lens, int num_seqs, int Hq, int Hkv, int N,
+                                 int d, int block_size, int max_blocks_per_seq, int num_blocks,
+                                 float scale, void* o, float* lse, void* stream);
 
 /*
  * attn_get_device_status — synchronises `stream`, copies the current

@@ -302,7 +302,7 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale,
 
 
 def prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scale,
-                  block_size=16):
+                  block_size=16, rows=None):
     """Chunked prefill over a paged KV cache (plain definition).
 
     "Fast attention kernels and operator fusion accelerate AI models",
@@ -325,7 +325,10 @@ def prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scal
     q [S, Hq, N, d]; k_new / v_new [S, Hkv, N, d]; caches
     [num_blocks, Hkv, block_size, d] (not modified: updated copies are
     returned); block_table [S, max_blocks] int; ctx_lens [S] int.
-    Returns (o [S, Hq, N, d], lse [S, Hq, N], k_cache_out, v_cache_out), fp64.
+    ``rows`` optionally selects the new-query rows of step 3 (rows are
+    independent by definition, so a subset is exact for those rows).
+    Returns (o [S, Hq, R, d], lse [S, Hq, R], k_cache_out, v_cache_out) in
+    fp64, R = len(rows) (N by default).
     """
     q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
     kc = np.array(k_cache, dtype=np.float64, copy=True)
@@ -348,17 +351,18 @@ def prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens, scal
                 kc[phys, g, end % block_size:] = 0.0
                 vc[phys, g, end % block_size:] = 0.0
     # Step 3: attention of the new queries over the updated cache.
-    o = np.zeros((S, Hq, N, v_new.shape[3]))
-    lse = np.zeros((S, Hq, N))
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    o = np.zeros((S, Hq, rows.size, v_new.shape[3]))
+    lse = np.zeros((S, Hq, rows.size))
     for b in range(S):
         ctx = int(ctx_lens[b])
         n_keys = ctx + N
-        allowed = np.arange(n_keys)[None, :] <= (ctx + np.arange(N))[:, None]
+        allowed = np.arange(n_keys)[None, :] <= (ctx + rows)[:, None]
         for g in range(Hkv):
             kk = gather_paged_keys(kc, block_table[b], n_keys, g, block_size)
             vv = gather_paged_keys(vc, block_table[b], n_keys, g, block_size)
             for h in range(g * group, (g + 1) * group):
-                s = score_matrix(q[b, h], kk, scale)
+                s = score_matrix(q[b, h, rows], kk, scale)
                 p, m, l = softmax_probs(s, allowed)
                 o[b, h] = p @ vv
                 lse[b, h] = m + np.log(l)

@@ -37,8 +37,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for required in ("attn_fwd", "attn_decode_paged", "attn_decode_paged_workspace_size",
-                     "attn_get_device_status", "attn_status_string"):
+    for required in ("attn_fwd", "attn_bwd", "attn_decode_paged", "attn_decode_paged_workspace_size",
+                     "attn_prefill_paged", "attn_get_device_status", "attn_status_string"):
         assert required in names
 
 
@@ -49,7 +49,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert attn.abi_version() == 1
+    assert attn.abi_version() == 2
     assert attn.status_string(0) == "ATTN_OK"
     assert attn.status_string(5) == "ATTN_ERR_WORKSPACE"
 
@@ -87,6 +87,23 @@ def test_decode_host_validation(lib):
     assert _dec(lib, ws_bytes=16) == WORKSPACE
     assert _dec(lib, ws=ctypes.c_void_p(0)) == INVALID
     assert _dec(lib, S=0) == OK
+
+
+def _pre(lib, S=2, Hq=12, Hkv=2, N=64, d=128, bs=16, mb=8, nb=16, q=FAKE, kc=FAKE):
+    return lib.attn_prefill_paged(q, FAKE, FAKE, kc, FAKE, FAKE, FAKE, S, Hq, Hkv, N, d, bs, mb, nb,
+                                  0.1, FAKE, None, None)
+
+
+def test_prefill_paged_host_validation(lib):
+    assert _pre(lib, bs=32) == UNSUPPORTED
+    assert _pre(lib, d=96) == UNSUPPORTED
+    assert _pre(lib, Hq=12, Hkv=5) == INVALID
+    assert _pre(lib, N=-1) == INVALID
+    assert _pre(lib, N=129, mb=8) == INVALID                    # 129 new tokens > 8 blocks
+    assert _pre(lib, kc=ctypes.c_void_p(0)) == INVALID
+    assert _pre(lib, q=ctypes.c_void_p(0x10004)) == INVALID     # misaligned
+    assert _pre(lib, S=0) == OK
+    assert _pre(lib, N=0) == OK
 
 
 def test_workspace_size_formula(lib):
