@@ -439,18 +439,12 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
 
+  // Q goes through TMA; the kernel gathers the cached K/V blocks itself.
   const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(attn47::fwd_box_rows()), 1};
   const cuuint64_t qdims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                                static_cast<cuuint64_t>(num_seqs) * Hq};
-  // The cache as [num_blocks][Hkv][16][d]: one box is the 16 slots of one
-  // (block, KV head), 64 columns wide.
-  const cuuint32_t cbox[4] = {64, 16, 1, 1};
-  const cuuint64_t cdims[4] = {static_cast<cuuint64_t>(d), 16, static_cast<cuuint64_t>(Hkv),
-                               static_cast<cuuint64_t>(num_blocks)};
-  alignas(64) CUtensorMap tq, tk, tv;
+  alignas(64) CUtensorMap tq;
   if ((st = encode_bf16(&tq, q, 3, qdims, qbox)) != ATTN_OK) return st;
-  if ((st = encode_bf16(&tk, k_cache, 4, cdims, cbox)) != ATTN_OK) return st;
-  if ((st = encode_bf16(&tv, v_cache, 4, cdims, cbox)) != ATTN_OK) return st;
 
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   attn47::AppendLaunch w;
@@ -474,8 +468,8 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
 
   attn47::FwdLaunch a;
   a.tq = &tq;
-  a.tk = &tk;
-  a.tv = &tv;
+  a.tk = &tq;   // unused in paged mode
+  a.tv = &tq;
   a.o = o;
   a.lse = lse;
   a.B = num_seqs;
@@ -490,6 +484,8 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
   a.timeout_ns = g_timeout_ns;
   a.stream = s;
   a.paged = true;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
   a.block_table = block_table;
   a.ctx_lens = ctx_lens;
   a.max_blocks = max_blocks_per_seq;

@@ -13,7 +13,8 @@
 //   warps 4-7   softmax of tile B
 //   warp 8      TMA producer: Q_A, Q_B once, then K_j / V_j into a stage ring
 //   warp 9      MMA issuer (one thread) and owner of the TMEM allocation
-//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg);
+//               in paged mode they gather the K and V tiles
 // Tensor memory: S_A, S_B (128 fp32 columns each), O_A, O_B (d columns
 // each).  After reading S_X, the softmax writes P_X (bf16, two per column)
 // over the first 64 columns of S_X and the MMA reads it from there (A
@@ -37,13 +38,19 @@
 // section: the cache lives in fixed-size blocks and every position goes
 // through the block table): the N query rows of sequence b are its new
 // tokens at positions ctx_b .. ctx_b + N - 1, and K/V come from the cache.
-// A 128-key tile is eight 16-slot blocks; the producer looks each one up in
-// the table and loads it as its own 16-row TMA box into the same swizzled
-// tile (the 128-byte swizzle repeats every 8 rows, so eight 16-row boxes at
-// 2 KB steps land exactly where one 128-row box would).  Blocks past the
-// sequence use a block index outside the pool, which the TMA unit fills
-// with zeros.  Query row i may see keys 0 .. ctx_b + i: the causal mask at an
-// offset, so it can fall across two key tiles.
+// A 128-key tile is eight 16-slot blocks of 16 x d contiguous values each.
+// Warps 10 (K) and 11 (V), idle otherwise, gather them: the lanes look up
+// the eight table entries, then copy each block with 16-byte cp.async
+// (a warp instruction moves 512 contiguous bytes) straight into the
+// 128-byte-swizzled tile layout the MMA descriptors read, wait for their
+// copies, fence them into the async proxy and arrive on the stage's full
+// barrier.  (Sixteen 16-row TMA boxes per tile took about a quarter longer
+// per tile than this.)  Blocks past the sequence are written as zeros.
+// Query row i may see keys 0 .. ctx_b + i: the causal mask at an offset, so
+// it can fall across two key tiles.  A unit's cost grows with
+// ctx_b + its query block's first row, so units are walked in decreasing
+// order of that key (every CTA ranks the (sequence, query block) pairs the
+// same way at start-up) instead of query block by query block.
 #include <cuda_runtime.h>
 
 #include "fwd_sm103.h"
@@ -81,7 +88,9 @@ struct FwdLayout {
   static constexpr int kOffK = kOffQ + kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStages * kKV;
   static constexpr int kOffBar = kOffV + kStages * kKV;
-  static constexpr int kSmem = kOffBar + 512 + 1024;     // barriers + alignment slack
+  static constexpr int kOffCtx = kOffBar + 512;          // paged: ctx_b of each sequence
+  static constexpr int kOffOrder = kOffCtx + 4 * 256;    // paged: (b << 16 | qblk) of each cost rank
+  static constexpr int kSmem = kOffOrder + 4 * 2048 + 1024;   // + alignment slack
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
 };
@@ -104,16 +113,25 @@ struct FwdParams {
   unsigned int* status;
   unsigned long long timeout_ns;
   // paged mode only
+  const uint8_t* k_cache;   // [num_blocks, Hkv, 16, D] bf16
+  const uint8_t* v_cache;
   const int* block_table;   // [B, max_blocks]
   const int* ctx_lens;      // [B] tokens cached before the N new ones
   int max_blocks, num_blocks;
   int max_ctx;              // max_blocks * 16 - N: largest valid ctx_lens entry
 };
 
+// Cost ordering of the paged mode fits in shared memory up to these sizes
+// (beyond them a second instantiation keeps the query-block-major order).
+constexpr int kSortMaxSeqs = 256;
+constexpr int kSortMaxPairs = 2048;
+
 constexpr int kPageRows = 16;                        // token slots per cache block
 constexpr int kPagesPerTile = kBN / kPageRows;
+constexpr int kWarpGatherK = 10;                     // paged mode: K / V gather warps
+constexpr int kWarpGatherV = 11;
 
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, bool PAGED, bool SORTED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk,
@@ -144,10 +162,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int qblk, zq, zkv, nA, nB;
     int pos0, b, kvh, nblk;                            // paged: ctx_b, sequence, KV head, blocks
   };
+  const int* s_ctx = reinterpret_cast<const int*>(smem + L::kOffCtx);
+  const int* s_order = reinterpret_cast<const int*>(smem + L::kOffOrder);
   auto unit_info = [&](int k) {
     Unit u;
-    u.qblk = p.num_q_blocks - 1 - k / p.bh_total;
-    const int bh = k % p.bh_total;
+    int bh;
+    if constexpr (SORTED) {
+      // Rank k / Hq of the (sequence, query block) pairs by decreasing cost;
+      // the Hq heads of a pair are consecutive units (they share K/V tiles).
+      const int r = k / p.Hq;
+      const int e = s_order[r];
+      u.qblk = e & 0xffff;
+      bh = (e >> 16) * p.Hq + (k - r * p.Hq);
+    } else {
+      u.qblk = p.num_q_blocks - 1 - k / p.bh_total;
+      bh = k % p.bh_total;
+    }
     u.zq = bh;                                         // b * Hq + h
     u.b = bh / p.Hq;
     u.kvh = (bh % p.Hq) / p.group;
@@ -178,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_addr(&bar->o_free[x]), 4);
     }
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(smem_addr(&bar->k_full[s]), 1);
-      mbar_init(smem_addr(&bar->v_full[s]), 1);
+      // Paged: every lane of a gather warp arrives once its copies landed.
+      mbar_init(smem_addr(&bar->k_full[s]), PAGED ? 32 : 1);
+      mbar_init(smem_addr(&bar->v_full[s]), PAGED ? 32 : 1);
       mbar_init(smem_addr(&bar->k_empty[s]), 1);
       mbar_init(smem_addr(&bar->v_empty[s]), 1);
     }
@@ -195,6 +226,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (SORTED) {
+    {
+      // Cost key of pair (b, qblk): ctx_b + 256 * qblk (the K/V tiles of the
+      // unit grow with it).  Rank = pairs with a larger key, plus equal keys
+      // of a smaller pair index; counted per sequence in closed form.
+      const int S = p.bh_total / p.Hq;
+      const int nq = p.num_q_blocks;
+      int* ctx_w = reinterpret_cast<int*>(smem + L::kOffCtx);
+      for (int b = threadIdx.x; b < S; b += kThreads) ctx_w[b] = min(max(__ldg(p.ctx_lens + b), 0), p.max_ctx);
+      __syncthreads();
+      int* order_w = reinterpret_cast<int*>(smem + L::kOffOrder);
+      for (int i = threadIdx.x; i < S * nq; i += kThreads) {
+        const int key = s_ctx[i / nq] + kRowsPerCta * (i % nq);
+        int rank = 0;
+        for (int b = 0; b < S; ++b) {
+          const int dk = key - s_ctx[b];
+          if (dk < 0) {
+            rank += nq;                            // every block of b has a larger key
+          } else {
+            const int q0 = dk / kRowsPerCta;       // blocks above q0 have larger keys
+            rank += max(nq - q0 - 1, 0);
+            if (dk % kRowsPerCta == 0 && q0 < nq && b * nq + q0 < i) ++rank;
+          }
+        }
+        order_w[rank] = ((i / nq) << 16) | (i % nq);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -228,43 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         u.qblk * kRowsPerCta + x * kBM, u.zq);
         };
         load_q(0);
+        if constexpr (PAGED) {                     // K/V come from the gather warps
+          if (ok) load_q(1);
+        }
         // K/V tiles: one stage ring for the whole CTA, across units.
-        for (int j = 0; j < u.nB && ok; ++j) {
+        for (int j = 0; j < (PAGED ? 0 : u.nB) && ok; ++j) {
           const int g = kv_issued + j;
           const int st = g % L::kStages;
           const uint32_t ph = (g / L::kStages) & 1;
-          // Paged: the physical blocks of this tile (read before the wait, so
-          // the table lookups overlap it); p.num_blocks lies outside the pool.
-          int page[PAGED ? kPagesPerTile : 1];
-          if constexpr (PAGED) {
-            const int* row = p.block_table + static_cast<size_t>(u.b) * p.max_blocks;
-#pragma unroll
-            for (int i = 0; i < kPagesPerTile; ++i) {
-              const int lb = j * kPagesPerTile + i;
-              page[i] = lb < u.nblk ? __ldg(row + lb) : p.num_blocks;
-            }
-#pragma unroll
-            for (int i = 0; i < kPagesPerTile; ++i) {
-              // An entry outside the pool is reported and read as zeros.
-              if (j * kPagesPerTile + i < u.nblk &&
-                  static_cast<unsigned>(page[i]) >= static_cast<unsigned>(p.num_blocks)) {
-                atomicOr(p.status, kDevBadBlock);
-                page[i] = p.num_blocks;
-              }
-            }
-          }
           auto load_kv = [&](uint32_t dst, const CUtensorMap* map, uint32_t full) {
             mbar_arrive_expect_tx(full, L::kKV);
-            if constexpr (PAGED) {
-#pragma unroll
-              for (int i = 0; i < kPagesPerTile; ++i)
-                for (int c = 0; c < L::kChunks; ++c)
-                  tma_load_4d(dst + c * L::kKVChunk + i * kPageRows * 128, map, full, c * 64, 0, u.kvh,
-                              page[i]);
-            } else {
-              for (int c = 0; c < L::kChunks; ++c)
-                tma_load_3d(dst + c * L::kKVChunk, map, full, c * 64, j * kBN, u.zkv);
-            }
+            for (int c = 0; c < L::kChunks; ++c)
+              tma_load_3d(dst + c * L::kKVChunk, map, full, c * 64, j * kBN, u.zkv);
           };
           if (!(ok = mbar_wait(smem_addr(&bar->k_empty[st]), ph ^ 1, wc))) break;
           load_kv(sK + st * L::kKV, &tk, smem_addr(&bar->k_full[st]));
@@ -441,6 +475,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       // All issued MMAs must retire before TMEM is released.
       umma_commit_warp(smem_addr(&bar->mma_final));
       __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
+    }
+  }
+  if constexpr (PAGED) {
+    if (warp == kWarpGatherK || warp == kWarpGatherV) {
+      // ------------------------------------------------- paged K / V gather
+      const bool is_v = warp == kWarpGatherV;
+      const uint8_t* cache = is_v ? p.v_cache : p.k_cache;
+      const uint32_t s_base = is_v ? sV : sK;
+      const uint32_t full0 = smem_addr(is_v ? &bar->v_full[0] : &bar->k_full[0]);
+      const uint32_t empty0 = smem_addr(is_v ? &bar->v_empty[0] : &bar->k_empty[0]);
+      constexpr int kRowPieces = D / 8;                        // 16-byte pieces of one key row
+      constexpr int kPerLane = kPageRows * kRowPieces / 32;    // pieces of one block per lane
+      const size_t slice_bytes = static_cast<size_t>(kPageRows) * D * 2;
+      int g = 0;                                               // fill index of the stage ring
+      bool ok = true;
+      for (int band = 0; ok; ++band) {
+        const int k = unit_at(band);
+        if (k >= p.num_units) break;
+        const Unit u = unit_info(k);
+        const int* row = p.block_table + static_cast<size_t>(u.b) * p.max_blocks;
+        for (int j = 0; j < u.nB; ++j, ++g) {
+          // Lane i < 8 translates block i of the tile (before the wait, so the
+          // lookup overlaps it); p.num_blocks stands for "no block": zeros.
+          int e = p.num_blocks;
+          const int lb = j * kPagesPerTile + lane;
+          if (lane < kPagesPerTile && lb < u.nblk) {
+            e = __ldg(row + lb);
+            if (static_cast<unsigned>(e) >= static_cast<unsigned>(p.num_blocks)) {
+              atomicOr(p.status, kDevBadBlock);                // reported, read as zeros
+              e = p.num_blocks;
+            }
+          }
+          const int st = g % L::kStages;
+          if (!(ok = mbar_wait_warp(empty0 + 8u * st, ((g / L::kStages) & 1) ^ 1, wc))) break;
+          const uint32_t dst0 = s_base + st * L::kKV;
+#pragma unroll 1
+          for (int i = 0; i < kPagesPerTile; ++i) {
+            const int phys = __shfl_sync(0xffffffffu, e, i);
+            const bool valid = phys < p.num_blocks;
+            const uint8_t* src0 = cache + (static_cast<size_t>(valid ? phys : 0) * p.Hkv + u.kvh) * slice_bytes;
+#pragma unroll
+            for (int t = 0; t < kPerLane; ++t) {
+              const int piece = t * 32 + lane;                 // consecutive lanes: consecutive 16 B
+              const int slot = piece / kRowPieces;
+              const int col = piece % kRowPieces;
+              // 128-byte swizzle: 16-byte column (col & 7) of row r sits at (col & 7) ^ (r & 7).
+              const uint32_t dst = dst0 + (col >> 3) * L::kKVChunk + (i * kPageRows + slot) * 128 +
+                                   ((static_cast<uint32_t>((col & 7) ^ (slot & 7))) << 4);
+              cp_async16(dst, src0 + piece * 16, valid ? 16u : 0u);
+            }
+          }
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+          mbar_arrive(full0 + 8u * st);
+        }
+      }
     }
   }
     // Each role ends on the same named barrier, so the register-split
@@ -636,10 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool PAGED>
+template <int D, bool CAUSAL, bool PAGED, bool SORTED = false>
 cudaError_t launch_t(const FwdLaunch& a) {
   using L = FwdLayout<D>;
-  auto kern = attn_fwd_sm103_kernel<D, CAUSAL, PAGED>;
+  auto kern = attn_fwd_sm103_kernel<D, CAUSAL, PAGED, SORTED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
   FwdParams p;
@@ -655,6 +745,8 @@ cudaError_t launch_t(const FwdLaunch& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
+  p.k_cache = static_cast<const uint8_t*>(a.k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a.v_cache);
   p.block_table = a.block_table;
   p.ctx_lens = a.ctx_lens;
   p.max_blocks = a.max_blocks;
@@ -671,7 +763,12 @@ cudaError_t launch_t(const FwdLaunch& a) {
 int fwd_box_rows() { return kBM; }
 
 cudaError_t launch_fwd_sm103(const FwdLaunch& a) {
-  if (a.paged) return a.d == 128 ? launch_t<128, true, true>(a) : launch_t<64, true, true>(a);
+  if (a.paged) {
+    const long long pairs = static_cast<long long>(a.B) * ((a.N + kRowsPerCta - 1) / kRowsPerCta);
+    if (a.B <= kSortMaxSeqs && pairs <= kSortMaxPairs)
+      return a.d == 128 ? launch_t<128, true, true, true>(a) : launch_t<64, true, true, true>(a);
+    return a.d == 128 ? launch_t<128, true, true, false>(a) : launch_t<64, true, true, false>(a);
+  }
   if (a.d == 128) return a.causal ? launch_t<128, true, false>(a) : launch_t<128, false, false>(a);
   return a.causal ? launch_t<64, true, false>(a) : launch_t<64, false, false>(a);
 }

@@ -9,7 +9,7 @@ namespace attn47 {
 
 struct FwdLaunch {
   const CUtensorMap* tq;   // [B*Hq, N, d] bf16, box {64, fwd_box_rows(), 1}, 128-byte swizzle
-  const CUtensorMap* tk;   // [B*Hkv, N, d]; paged: cache [num_blocks, Hkv, 16, d], box {64, 16, 1, 1}
+  const CUtensorMap* tk;   // [B*Hkv, N, d] (not read in paged mode)
   const CUtensorMap* tv;   // same as tk
   void* o;                 // [B, Hq, N, d] bf16
   float* lse;              // [B, Hq, N] fp32 or nullptr
@@ -24,6 +24,8 @@ struct FwdLaunch {
   // sequence b sit at positions ctx_lens[b] .. ctx_lens[b] + N - 1 and K/V
   // come from the paged cache through block_table.
   bool paged = false;
+  const void* k_cache = nullptr;      // [num_blocks, Hkv, 16, d] bf16
+  const void* v_cache = nullptr;
   const int* block_table = nullptr;   // [B, max_blocks] int32
   const int* ctx_lens = nullptr;      // [B] int32
   int max_blocks = 0, num_blocks = 0;

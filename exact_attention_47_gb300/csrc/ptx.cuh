@@ -1,4 +1,4 @@
-// Inline-PTX helpers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
+// Inline-PTX helpers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor), cp.async,
 // tcgen05 (TMEM alloc / MMA / ld / st / commit), and the warp-level
 // mma.sync + ldmatrix used by the decode kernel.  Written from the PTX ISA.
 #pragma once
@@ -216,14 +216,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
-                                            int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
 // Contiguous global -> shared bulk copy (addresses 16-byte aligned, size a
 // multiple of 16), completing on `bar` with complete_tx.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -249,6 +241,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait_primary() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// 16-byte asynchronous global -> shared copy through L2 (cp.async.cg).  With
+// src_bytes = 0 it writes 16 zero bytes and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+// Wait until every cp.async this thread issued has written shared memory.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

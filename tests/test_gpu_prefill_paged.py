@@ -172,3 +172,17 @@ def test_empty_chunk_launches_nothing():
     o, lse, dx = _gpu(x, 0.125)
     assert o.numel() == 0 and lse.numel() == 0
     assert torch.equal(dx["k_cache"].cpu().view(torch.int16), before.view(torch.int16))
+
+
+def test_many_sequences_keep_query_block_order():
+    """More sequences than the start-up cost ranking holds (257 > 256): the
+    kernel walks the units in query-block order instead; same results."""
+    S, Hq, Hkv, N, d = 257, 2, 1, 3, 64
+    ctx = [(7 * b) % 41 for b in range(S)]
+    x = workloads.paged_prefill_inputs(S, Hq, Hkv, N, d, seed=76, ctx_lens=ctx)
+    scale = workloads.default_scale(d)
+    o, lse, dx = _gpu(x, scale)
+    assert attn.device_status() == 0
+    ro, rl, rk, _ = _ref(x, scale)
+    assert_attn_close(o, lse, ro, rl, what="257 sequences")
+    _assert_cache_equal(dx["k_cache"], rk, "k_cache")
