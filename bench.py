@@ -5,6 +5,12 @@ One step = one pass of the whole path over one batch of synthetic input:
                      N=4096, d=128, causal, bf16 (one launch)
   attn_decode_paged  64 sequences, Hq=12, Hkv=2, d=128, block_size 16,
                      lengths U[128, 4096], permuted block table (two launches)
+Also timed, outside the step and reported under their own keys:
+  fwd_configs        attn_fwd on the GPT-2-small-shaped and long-context prefill
+  backward           attn_bwd (dQ, dK, dV) on the Qwen-style prefill
+  paged_prefill      attn_prefill_paged: 2048 new tokens per sequence on top of
+                     a cached prefix of U[0, 6144] tokens (4 sequences,
+                     Qwen-style GQA, block_size 16, permuted table)
 Printed (rank 0, one JSON line): fwd TFLOP/s as `value` (causal flops
 4*B*Hq*N^2*d/2 over the forward kernel's CUDA-event time), the decode's HBM
 GB/s (algorithmic bytes over its kernels' time) under "decode", rooflines
