@@ -10,13 +10,15 @@ Sources (web pages, cited by title and section):
     "Flash Attention", "Tiling" (steps 1–3), "Softmax stabiliser",
     "Incremental / online softmax".
   * "Fast attention kernels and operator fusion accelerate AI models":
-    section "FlashAttention-style attention and Paged Attention".
+    sections "FlashAttention-style attention and Paged Attention" and
+    "Operator fusion" (``fusions.py``: residual add + RMSNorm, SwiGLU).
 
 Every function here is pinned against brute force, closed forms, a library
 routine and invariants the mathematics fixes: the forward and decode by
 ``tests/test_oracle_pins.py``, the backward by
 ``tests/test_oracle_backward_pins.py``, the chunked prefill over a paged
-cache by ``tests/test_oracle_paged_prefill_pins.py``.  No function is
+cache by ``tests/test_oracle_paged_prefill_pins.py``, the fusions by
+``tests/test_oracle_fusion_pins.py``.  No function is
 "parity unpinned".
 """
 
@@ -32,3 +34,4 @@ from .definitions import (  # noqa: F401
     softmax_probs,
     split_partials,
 )
+from .fusions import add_rmsnorm, round_bf16, swiglu  # noqa: F401

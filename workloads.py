@@ -177,3 +177,30 @@ def paged_prefill_inputs(num_seqs, Hq, Hkv, N_new, d, seed, ctx_lo=0, ctx_hi=409
                 block_table=table, ctx_lens=ctx_lens.to(torch.int32), k_prefix=k_prefix,
                 v_prefix=v_prefix, block_size=block_size,
                 max_blocks_per_seq=max_blocks_per_seq, num_blocks=num_blocks)
+
+
+FUSION_CONFIGS = {
+    # One Qwen2.5-1.5B-sized layer over the 4 x 4096 tokens of the prefill
+    # workload: hidden size 1536, MLP intermediate size 8960.
+    "qwen_add_rmsnorm": dict(rows=16384, hidden=1536, seed=6),
+    "qwen_swiglu": dict(rows=16384, F=8960, seed=7),
+}
+
+
+def add_rmsnorm_inputs(rows, hidden, seed):
+    """x, residual [rows, hidden] ~ N(0, 1) and weight [hidden] ~ N(1, 0.1^2), bf16 (CPU)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    x = _randn(gen, (rows, hidden)).to(torch.bfloat16)
+    residual = _randn(gen, (rows, hidden)).to(torch.bfloat16)
+    weight = (1.0 + 0.1 * _randn(gen, (hidden,))).to(torch.bfloat16)
+    return x, residual, weight
+
+
+def swiglu_inputs(rows, F, seed):
+    """Merged gate/up projection output [rows, 2F] bf16 (CPU): gate columns
+    ~ N(0, 2^2) (so SiLU sees both its linear and its vanishing side), up
+    columns ~ N(0, 1)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    g = _randn(gen, (rows, F), 2.0)
+    u = _randn(gen, (rows, F))
+    return torch.cat([g, u], dim=1).to(torch.bfloat16)
