@@ -11,6 +11,8 @@ Also timed, outside the step and reported under their own keys:
   paged_prefill      attn_prefill_paged: 2048 new tokens per sequence on top of
                      a cached prefix of U[0, 6144] tokens (4 sequences,
                      Qwen-style GQA, block_size 16, permuted table)
+  fusions            fused_add_rmsnorm and fused_swiglu on a Qwen2.5-1.5B-sized
+                     layer over 16384 tokens (HBM GB/s)
 Printed (rank 0, one JSON line): fwd TFLOP/s as `value` (causal flops
 4*B*Hq*N^2*d/2 over the forward kernel's CUDA-event time), the decode's HBM
 GB/s (algorithmic bytes over its kernels' time) under "decode", rooflines
@@ -51,8 +53,10 @@ NSETS = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
 # ncu summaries (profiles/), taken on this workload; None once a kernel changes
-# until it is captured again.  Decode: main kernel + merge kernel.
-TRAFFIC_FWD = 67189504 + 7851008
+# until it is captured again.  Forward: medians over the 10 launches of the
+# bench step in one capture (reads are q + k + v; writes vary with what o and
+# lse leave in L2).  Decode: main kernel + merge kernel.
+TRAFFIC_FWD = 67192448 + 4752640
 TRAFFIC_DEC = (132292096 + 3670272) + (3272704 + 0)
 
 
@@ -387,6 +391,52 @@ def paged_prefill_measurement(attn, device, steps, peak):
             "kernels": "kv append + attention (paged mode)", "gpu_launches_per_call": 2}
 
 
+def fusion_measurement(attn, device, steps, peak_gbs):
+    """fused_add_rmsnorm and fused_swiglu on one Qwen2.5-1.5B-sized layer over
+    the 16384 prefill tokens (hidden 1536, intermediate 8960), CUDA events over
+    `steps` calls after 3 warm-ups.  Algorithmic bytes: every input read once,
+    every output written once (add + RMSNorm: x, residual in; residual, out
+    out; swiglu: [rows, 2F] in, [rows, F] out).  Two input sets alternate for
+    add + RMSNorm (2 x 151 MB > L2); one swiglu call moves 881 MB."""
+    c = workloads.FUSION_CONFIGS["qwen_add_rmsnorm"]
+    sets = []
+    for i in range(2):
+        x, res, w = workloads.add_rmsnorm_inputs(c["rows"], c["hidden"], c["seed"] + 100 * i)
+        sets.append((x.to(device), res.to(device), w.to(device), torch.empty_like(x, device=device)))
+    nbytes = 4 * c["rows"] * c["hidden"] * 2 + c["hidden"] * 2
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, n):
+        for i in range(3):
+            fn(i)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    ms_norm = timed(lambda i: attn.fused_add_rmsnorm(sets[i % 2][0], sets[i % 2][1], sets[i % 2][2],
+                                                     out=sets[i % 2][3]), steps)
+    del sets
+    g = workloads.FUSION_CONFIGS["qwen_swiglu"]
+    gu = workloads.swiglu_inputs(g["rows"], g["F"], g["seed"]).to(device)
+    out = torch.empty((g["rows"], g["F"]), dtype=torch.bfloat16, device=device)
+    gbytes = 3 * g["rows"] * g["F"] * 2
+    ms_glu = timed(lambda i: attn.fused_swiglu(gu, out=out), steps)
+    del gu, out
+    res = {}
+    for name, ms, b, shape in (("add_rmsnorm", ms_norm, nbytes, "rows 16384 hidden 1536"),
+                               ("swiglu", ms_glu, gbytes, "rows 16384 F 8960")):
+        gbs = b / (ms / 1e3) / 1e9
+        res[name] = {"shape": shape, "ms": ms, "bytes": b, "GB/s": gbs, "frac": gbs / peak_gbs,
+                     "bound": "hbm"}
+    return res
+
+
 def run_gpu(args, rank, world, local_rank):
     import exact_attention_47_gb300 as attn
 
@@ -490,6 +540,7 @@ def run_gpu(args, rank, world, local_rank):
     fwd_configs = fwd_config_table(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
     backward = bwd_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
     paged_prefill = paged_prefill_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
+    fusions = fusion_measurement(attn, device, max(10, K // 2), pk_all["hbm_gbs"])
 
     # ---- max over ranks
     total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
@@ -530,6 +581,7 @@ def run_gpu(args, rank, world, local_rank):
                 "tflops": achieved_fwd, "frac": achieved_fwd / pk["bf16_tflops"]}}),
             "backward": backward,
             "paged_prefill": paged_prefill,
+            "fusions": fusions,
             "gpu_launches": 3 * K,
             "clocks": clock.summary(wall0, wall1),
         }

@@ -1,5 +1,6 @@
 """GB300 (sm_103a) exact attention: tiled online-softmax prefill, its backward,
-paged-KV decode and chunked prefill over the paged cache.
+paged-KV decode, chunked prefill over the paged cache, and the residual
+add + RMSNorm and SwiGLU fusions of the same layer.
 
 The compute lives in ``lib/libattn47_sm103.so`` (hand-written CUDA, C-ABI
 declared in ``include/attn47.h``); this package is its Python binding.
@@ -22,6 +23,8 @@ from ._binding import (  # noqa: F401
     attn_fwd,
     attn_prefill_paged,
     device_status,
+    fused_add_rmsnorm,
+    fused_swiglu,
     library_path,
     load_library,
     selftest_wait_timeout,

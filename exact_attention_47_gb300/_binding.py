@@ -36,6 +36,8 @@ _SIGS = {
                                        _P, _P, _P]),
     "attn_prefill_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                 ctypes.c_float, _P, _P, _P]),
+    "fused_add_rmsnorm": (_I, [_P, _P, _P, _P, _I, _I, ctypes.c_float, _P]),
+    "fused_swiglu": (_I, [_P, _P, _I, _I, _P]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
@@ -311,6 +313,47 @@ def attn_prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens,
                                 _stream_handle(stream))
     _check("attn_prefill_paged", st)
     return o, lse
+
+
+def fused_add_rmsnorm(x, residual, weight, eps=1e-6, out=None, stream=None):
+    """Residual add + RMSNorm.  x, residual [rows, hidden] and weight [hidden]
+    bf16 on the GPU; ``residual`` is overwritten with bf16(x + residual).
+    Returns (out [rows, hidden] bf16, residual)."""
+    lib = load_library()
+    for name, t in (("x", x), ("residual", residual), ("weight", weight)):
+        _need_cuda(name, t, torch.bfloat16)
+    if x.dim() != 2 or residual.shape != x.shape or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
+        raise ValueError("x and residual must be [rows, hidden] and weight [hidden]")
+    rows, hidden = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        if out.shape != x.shape:
+            raise ValueError("out must have x's shape")
+    st = lib.fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), _ptr(out), rows, hidden,
+                               float(eps), _stream_handle(stream))
+    _check("fused_add_rmsnorm", st)
+    return out, residual
+
+
+def fused_swiglu(gate_up, out=None, stream=None):
+    """SwiGLU activation of the merged gate/up projection output
+    gate_up [rows, 2F] bf16 (gate first): returns silu(gate) * up [rows, F] bf16."""
+    lib = load_library()
+    _need_cuda("gate_up", gate_up, torch.bfloat16)
+    if gate_up.dim() != 2 or gate_up.shape[1] % 2 != 0:
+        raise ValueError("gate_up must be [rows, 2F]")
+    rows, F = gate_up.shape[0], gate_up.shape[1] // 2
+    if out is None:
+        out = torch.empty((rows, F), dtype=torch.bfloat16, device=gate_up.device)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        if tuple(out.shape) != (rows, F):
+            raise ValueError("out must be [rows, F]")
+    st = lib.fused_swiglu(_ptr(gate_up), _ptr(out), rows, F, _stream_handle(stream))
+    _check("fused_swiglu", st)
+    return out
 
 
 def device_status(stream=None):

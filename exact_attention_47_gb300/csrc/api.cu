@@ -13,6 +13,7 @@
 #include "attn47.h"
 #include "decode_sm103.h"
 #include "bwd_sm103.h"
+#include "fusion_sm103.h"
 #include "fwd_sm103.h"
 #include "ptx.cuh"
 
@@ -101,6 +102,10 @@ attn_status_t current_device(DeviceInfo** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
 bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
 
 // bf16 tensor map over `rank` dims (innermost first), 64-column boxes,
@@ -491,6 +496,66 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
   a.max_blocks = max_blocks_per_seq;
   a.num_blocks = num_blocks;
   return launch_result(attn47::launch_fwd_sm103(a), "attn_prefill_paged (attention)");
+}
+
+attn_status_t fused_add_rmsnorm(const void* x, void* residual, const void* weight, void* out,
+                                int rows, int hidden, float eps, void* stream) {
+  if (rows < 0 || hidden < 8) return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy rows >= 0, hidden >= 8");
+  if (hidden % 8 != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "hidden (%d) must be a multiple of 8 (16-byte rows)", hidden);
+  if (!(std::isfinite(eps) && eps >= 0.f)) return fail(ATTN_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (rows == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!x || !residual || !weight || !out)
+    return fail(ATTN_ERR_INVALID_ARG, "x, residual, weight and out must be non-null");
+  if (!aligned16(x) || !aligned16(residual) || !aligned16(weight) || !aligned16(out))
+    return fail(ATTN_ERR_INVALID_ARG, "x, residual, weight and out must be 16-byte aligned");
+  const size_t bytes = static_cast<size_t>(rows) * hidden * 2;
+  if (overlap(residual, bytes, x, bytes) || overlap(residual, bytes, out, bytes) ||
+      overlap(out, bytes, x, bytes) || overlap(weight, static_cast<size_t>(hidden) * 2, residual, bytes) ||
+      overlap(weight, static_cast<size_t>(hidden) * 2, out, bytes))
+    return fail(ATTN_ERR_INVALID_ARG, "x, residual, weight and out must not overlap");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  attn47::NormLaunch a;
+  a.x = x;
+  a.residual = residual;
+  a.weight = weight;
+  a.out = out;
+  a.rows = rows;
+  a.hidden = hidden;
+  a.eps = eps;
+  a.sms = dev->sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_add_rmsnorm_sm103(a), "fused_add_rmsnorm");
+}
+
+attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void* stream) {
+  if (rows < 0 || F < 8) return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy rows >= 0, F >= 8");
+  if (F % 8 != 0) return fail(ATTN_ERR_UNSUPPORTED, "F (%d) must be a multiple of 8 (16-byte rows)", F);
+  if (rows == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!gate_up || !out) return fail(ATTN_ERR_INVALID_ARG, "gate_up and out must be non-null");
+  if (!aligned16(gate_up) || !aligned16(out))
+    return fail(ATTN_ERR_INVALID_ARG, "gate_up and out must be 16-byte aligned");
+  if (overlap(gate_up, static_cast<size_t>(rows) * F * 4, out, static_cast<size_t>(rows) * F * 2))
+    return fail(ATTN_ERR_INVALID_ARG, "gate_up and out must not overlap");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  attn47::GluLaunch a;
+  a.gate_up = gate_up;
+  a.out = out;
+  a.rows = rows;
+  a.F = F;
+  a.sms = dev->sms;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_swiglu_sm103(a), "fused_swiglu");
 }
 
 attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {

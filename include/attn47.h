@@ -2,7 +2,7 @@
  * attn47.h — C-ABI of the GB300 (sm_103a) exact-attention library
  * (libattn47_sm103.so).
  *
- * Four operations, all bf16 in / fp32 accumulate:
+ * Four attention operations, all bf16 in / fp32 accumulate:
  *
  *  attn_fwd           softmax(scale * Q K^T + causal mask) V for a whole
  *                     sequence (prefill), computed tile by tile with the
@@ -37,6 +37,13 @@
  *                     new tokens up to itself (same page and section: the
  *                     cache grows as tokens arrive; the serving example runs
  *                     prefill, then decode, over block_size = 16 blocks).
+ *
+ * and two operator fusions of the same transformer layer (same page,
+ * section "Operator fusion"):
+ *
+ *  fused_add_rmsnorm  residual add followed by RMSNorm, one pass
+ *  fused_swiglu       SwiGLU activation silu(gate) * up of the merged
+ *                     gate/up projection output, one pass
  *
  * Conventions shared by every call
  *  - Pointers are DEVICE pointers of the current CUDA device unless stated.
@@ -255,6 +262,51 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
                                  const int32_t* ctx_lens, int num_seqs, int Hq, int Hkv, int N,
                                  int d, int block_size, int max_blocks_per_seq, int num_blocks,
                                  float scale, void* o, float* lse, void* stream);
+
+/*
+ * fused_add_rmsnorm — residual add + RMSNorm in one kernel.
+ *
+ * "Fast attention kernels and operator fusion accelerate AI models",
+ * section "Operator fusion": adding the residual connection and then
+ * normalising with RMSNorm is a common fusion; fused, the sum is never
+ * written and re-read between two kernels.  For every row:
+ *   residual <- bf16(x + residual)                       (the new residual stream)
+ *   out      <- bf16(residual * rsqrt(mean(residual^2) + eps) * weight)
+ * where the mean runs over the `hidden` values of the row as stored (bf16),
+ * so the result is that of an unfused add kernel followed by RMSNorm.
+ *
+ *  x         [rows, hidden] bf16 (read)
+ *  residual  [rows, hidden] bf16 (read, then overwritten in place)
+ *  weight    [hidden] bf16
+ *  out       [rows, hidden] bf16 (written)
+ *  hidden must be a multiple of 8 (>= 8); eps finite and >= 0.  All pointers
+ *  16-byte aligned; the four buffers must not overlap (ATTN_ERR_INVALID_ARG).
+ *  rows == 0 is an empty problem: ATTN_OK, nothing launched.  One kernel,
+ *  one warp per row; deterministic.
+ */
+attn_status_t fused_add_rmsnorm(const void* x, void* residual, const void* weight, void* out,
+                                int rows, int hidden, float eps, void* stream);
+
+/*
+ * fused_swiglu — the SwiGLU activation in one kernel.
+ *
+ * "Fast attention kernels and operator fusion accelerate AI models",
+ * section "Operator fusion": the SwiGLU block, run naively, launches a SiLU
+ * kernel and an elementwise-product kernel between its projection matmuls,
+ * each writing its intermediate to HBM; fused, the gate/up projection output
+ * is read once and only the product is written:
+ *   out[r, j] = bf16(silu(g) * u),  silu(g) = g / (1 + exp(-g)),
+ *   g = gate_up[r, j],  u = gate_up[r, F + j].
+ * (The projection matmuls themselves are plain GEMMs and not part of this
+ * library.)
+ *
+ *  gate_up  [rows, 2F] bf16: the merged gate/up projection output, gate in
+ *           columns 0..F-1, up in columns F..2F-1
+ *  out      [rows, F] bf16 (written; must not overlap gate_up)
+ *  F must be a multiple of 8 (>= 8); both pointers 16-byte aligned.
+ *  rows == 0 is an empty problem.  One kernel; deterministic.
+ */
+attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void* stream);
 
 /*
  * attn_get_device_status — synchronises `stream`, copies the current

@@ -24,7 +24,7 @@ FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced on these paths
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:attn|fused)_[a-z_0-9]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -38,7 +38,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("attn_fwd", "attn_bwd", "attn_decode_paged", "attn_decode_paged_workspace_size",
-                     "attn_prefill_paged", "attn_get_device_status", "attn_status_string"):
+                     "attn_prefill_paged", "fused_add_rmsnorm", "fused_swiglu",
+                     "attn_get_device_status", "attn_status_string"):
         assert required in names
 
 
@@ -104,6 +105,18 @@ def test_prefill_paged_host_validation(lib):
     assert _pre(lib, q=ctypes.c_void_p(0x10004)) == INVALID     # misaligned
     assert _pre(lib, S=0) == OK
     assert _pre(lib, N=0) == OK
+
+
+def test_fusion_host_validation(lib):
+    assert lib.fused_add_rmsnorm(FAKE, ctypes.c_void_p(0x20000), FAKE, ctypes.c_void_p(0x30000), 4, 12, 1e-6, None) == UNSUPPORTED
+    assert lib.fused_add_rmsnorm(FAKE, ctypes.c_void_p(0x20000), FAKE, ctypes.c_void_p(0x30000), 4, 16, -1.0, None) == INVALID
+    assert lib.fused_add_rmsnorm(FAKE, FAKE, ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000), 4, 16, 1e-6, None) == INVALID  # x is residual
+    assert lib.fused_add_rmsnorm(FAKE, ctypes.c_void_p(0x20000), FAKE, ctypes.c_void_p(0x20010), 4, 16, 1e-6, None) == INVALID  # out overlaps residual
+    assert lib.fused_add_rmsnorm(FAKE, FAKE, FAKE, FAKE, 0, 16, 1e-6, None) == OK
+    assert lib.fused_swiglu(FAKE, ctypes.c_void_p(0x40000), 4, 12, None) == UNSUPPORTED
+    assert lib.fused_swiglu(FAKE, ctypes.c_void_p(0x10040), 4, 16, None) == INVALID              # out inside gate_up
+    assert lib.fused_swiglu(ctypes.c_void_p(0x10008), ctypes.c_void_p(0x40000), 4, 16, None) == INVALID
+    assert lib.fused_swiglu(FAKE, FAKE, 0, 16, None) == OK
 
 
 def test_workspace_size_formula(lib):
