@@ -12,13 +12,15 @@ Sources (web pages, cited by title and section):
   * "Fast attention kernels and operator fusion accelerate AI models":
     sections "FlashAttention-style attention and Paged Attention" and
     "Operator fusion" (``fusions.py``: residual add + RMSNorm, SwiGLU).
+  * "Accelerating Mamba-2 with high-performance forward kernels in NVIDIA
+    CUDA Tile" (``ssd.py``: the SSD recurrence and its chunked form).
 
 Every function here is pinned against brute force, closed forms, a library
 routine and invariants the mathematics fixes: the forward and decode by
 ``tests/test_oracle_pins.py``, the backward by
 ``tests/test_oracle_backward_pins.py``, the chunked prefill over a paged
 cache by ``tests/test_oracle_paged_prefill_pins.py``, the fusions by
-``tests/test_oracle_fusion_pins.py``.  No function is
+``tests/test_oracle_fusion_pins.py``, the SSD by ``tests/test_oracle_ssd_pins.py``.  No function is
 "parity unpinned".
 """
 
@@ -35,3 +37,10 @@ from .definitions import (  # noqa: F401
     split_partials,
 )
 from .fusions import add_rmsnorm, round_bf16, swiglu  # noqa: F401
+from .ssd import (  # noqa: F401
+    ssd_chunk_cumsum,
+    ssd_chunk_output,
+    ssd_chunked,
+    ssd_fwd_pass_state,
+    ssd_recurrence,
+)

@@ -204,3 +204,24 @@ def swiglu_inputs(rows, F, seed):
     g = _randn(gen, (rows, F), 2.0)
     u = _randn(gen, (rows, F))
     return torch.cat([g, u], dim=1).to(torch.bfloat16)
+
+
+SSD_CONFIGS = {
+    # A Mamba-2-2.7B-sized layer (d_model 2560, expand 2: 80 heads of 64,
+    # state 128, one group, chunk 256) over 4 sequences of 4096 tokens.
+    "mamba2_ssd": dict(batch=4, L=4096, H=80, P=64, N=128, G=1, chunk=256, seed=8),
+}
+
+
+def ssd_inputs(batch, L, H, P, N, G, seed):
+    """Mamba-2 SSD inputs (CPU): x [batch, L, H, P], B, C [batch, L, G, N] bf16
+    ~ N(0, 1); dt [batch, L, H] fp32 log-uniform in [1e-3, 1e-1]; A [H] fp32
+    = -exp(U[0, ln 16]) (decay rates in [1, 16], negative)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    x = _randn(gen, (batch, L, H, P)).to(torch.bfloat16)
+    B = _randn(gen, (batch, L, G, N)).to(torch.bfloat16)
+    C = _randn(gen, (batch, L, G, N)).to(torch.bfloat16)
+    lo, hi = math.log(1e-3), math.log(1e-1)
+    dt = torch.exp(lo + (hi - lo) * torch.rand((batch, L, H), generator=gen, dtype=torch.float32))
+    A = -torch.exp(math.log(16.0) * torch.rand((H,), generator=gen, dtype=torch.float32))
+    return dict(x=x, dt=dt, A=A, B=B, C=C)
