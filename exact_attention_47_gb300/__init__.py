@@ -30,5 +30,7 @@ from ._binding import (  # noqa: F401
     selftest_wait_timeout,
     set_decode_max_ctas,
     set_wait_timeout_ns,
+    ssd_chunked_fwd,
+    ssd_workspace_size,
     status_string,
 )

@@ -38,6 +38,9 @@ _SIGS = {
                                 ctypes.c_float, _P, _P, _P]),
     "fused_add_rmsnorm": (_I, [_P, _P, _P, _P, _I, _I, ctypes.c_float, _P]),
     "fused_swiglu": (_I, [_P, _P, _I, _I, _P]),
+    "ssd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "ssd_chunked_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                             ctypes.c_size_t, _P]),
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
@@ -354,6 +357,44 @@ def fused_swiglu(gate_up, out=None, stream=None):
     st = lib.fused_swiglu(_ptr(gate_up), _ptr(out), rows, F, _stream_handle(stream))
     _check("fused_swiglu", st)
     return out
+
+
+def ssd_workspace_size(batch, L, H, N, chunk):
+    return int(load_library().ssd_workspace_size(batch, L, H, N, chunk))
+
+
+def ssd_chunked_fwd(x, dt, A, B, C, chunk=256, h0=None, y=None, h_final=None, workspace=None,
+                    stream=None):
+    """Mamba-2 SSD forward.  x [batch, L, H, P] bf16, dt [batch, L, H] fp32,
+    A [H] fp32, B and C [batch, L, G, N] bf16, h0 [batch, H, P, N] fp32 or
+    None, all on the GPU.  Returns (y [batch, L, H, P] bf16, h_final
+    [batch, H, P, N] fp32)."""
+    lib = load_library()
+    for name, t, dtype in (("x", x, torch.bfloat16), ("dt", dt, torch.float32), ("A", A, torch.float32),
+                           ("B", B, torch.bfloat16), ("C", C, torch.bfloat16)):
+        _need_cuda(name, t, dtype)
+    if x.dim() != 4 or dt.dim() != 3 or A.dim() != 1 or B.dim() != 4 or C.shape != B.shape:
+        raise ValueError("x [batch, L, H, P], dt [batch, L, H], A [H], B/C [batch, L, G, N]")
+    batch, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if tuple(dt.shape) != (batch, L, H) or A.shape[0] != H or B.shape[:2] != x.shape[:2]:
+        raise ValueError("dt, A, B and C do not match x")
+    if h0 is not None:
+        _need_cuda("h0", h0, torch.float32)
+        if tuple(h0.shape) != (batch, H, P, N):
+            raise ValueError("h0 must be [batch, H, P, N]")
+    y = torch.empty_like(x) if y is None else y
+    h_final = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device) if h_final is None else h_final
+    _need_cuda("y", y, torch.bfloat16)
+    _need_cuda("h_final", h_final, torch.float32)
+    need = ssd_workspace_size(batch, L, H, N, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    st = lib.ssd_chunked_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(y), _ptr(h_final),
+                             batch, L, H, G, P, N, chunk, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check("ssd_chunked_fwd", st)
+    return y, h_final
 
 
 def device_status(stream=None):

@@ -15,6 +15,7 @@
 #include "bwd_sm103.h"
 #include "fusion_sm103.h"
 #include "fwd_sm103.h"
+#include "ssd_sm103.h"
 #include "ptx.cuh"
 
 // Per-device error word written by the kernels (ATTN_DEV_* bits).
@@ -556,6 +557,62 @@ attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void
   a.sms = dev->sms;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_result(attn47::launch_swiglu_sm103(a), "fused_swiglu");
+}
+
+size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk) {
+  if (batch <= 0 || L <= 0 || H <= 0 || N <= 0 || chunk <= 0) return 0;
+  return attn47::ssd_workspace_bytes(batch, L, H, N, chunk);
+}
+
+attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, const void* B,
+                              const void* C, const float* h0, void* y, float* h_final, int batch,
+                              int L, int H, int G, int P, int N, int chunk, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (batch < 0 || L < 0 || H < 1 || G < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy batch >= 0, L >= 0, H >= 1, G >= 1");
+  if (H % G != 0) return fail(ATTN_ERR_INVALID_ARG, "H (%d) is not a multiple of G (%d)", H, G);
+  if (P != attn47::ssd_head_dim()) return fail(ATTN_ERR_UNSUPPORTED, "head dim P = %d not supported (64)", P);
+  if (N != 64 && N != 128) return fail(ATTN_ERR_UNSUPPORTED, "state size N = %d not supported (64 or 128)", N);
+  if (chunk != 64 && chunk != 128 && chunk != 256)
+    return fail(ATTN_ERR_UNSUPPORTED, "chunk = %d not supported (64, 128 or 256)", chunk);
+  if (batch == 0 || L == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!x || !dt || !A || !B || !C || !y || !h_final || !workspace)
+    return fail(ATTN_ERR_INVALID_ARG, "x, dt, A, B, C, y, h_final and workspace must be non-null");
+  if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(y) || !aligned16(h_final) ||
+      !aligned16(workspace) || (h0 && !aligned16(h0)))
+    return fail(ATTN_ERR_INVALID_ARG, "x, B, C, y, h0, h_final and workspace must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(dt) & 3u) || (reinterpret_cast<uintptr_t>(A) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "dt and A must be 4-byte aligned");
+  const long long nc = (static_cast<long long>(L) + chunk - 1) / chunk;
+  if (static_cast<long long>(batch) * nc * H * (chunk / 64) > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  const size_t need = ssd_workspace_size(batch, L, H, N, chunk);
+  if (workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  attn47::SsdLaunch a;
+  a.x = x;
+  a.dt = dt;
+  a.A = A;
+  a.B = B;
+  a.C = C;
+  a.h0 = h0;
+  a.y = y;
+  a.h_final = h_final;
+  a.workspace = workspace;
+  a.batch = batch;
+  a.L = L;
+  a.H = H;
+  a.G = G;
+  a.N = N;
+  a.chunk = chunk;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_ssd_sm103(a), "ssd_chunked_fwd");
 }
 
 attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {

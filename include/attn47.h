@@ -45,6 +45,13 @@
  *  fused_swiglu       SwiGLU activation silu(gate) * up of the merged
  *                     gate/up projection output, one pass
  *
+ * and the Mamba-2 SSD forward ("Accelerating Mamba-2 with high-performance
+ * forward kernels in NVIDIA CUDA Tile"):
+ *
+ *  ssd_chunked_fwd    the state-space recurrence evaluated chunk by chunk
+ *                     (per-chunk cumulative decay, fwd_pass_state, chunk
+ *                     outputs)
+ *
  * Conventions shared by every call
  *  - Pointers are DEVICE pointers of the current CUDA device unless stated.
  *    The caller owns every buffer and the stream; the library allocates no
@@ -307,6 +314,45 @@ attn_status_t fused_add_rmsnorm(const void* x, void* residual, const void* weigh
  *  rows == 0 is an empty problem.  One kernel; deterministic.
  */
 attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void* stream);
+
+/*
+ * ssd_workspace_size — bytes of device workspace ssd_chunked_fwd needs: the
+ * per-chunk cumulative decays (fp32, batch * H * n_chunks * chunk) and every
+ * chunk's initial state (fp32, batch * n_chunks * H * 64 * N).  0 for an
+ * empty problem.
+ */
+size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk);
+
+/*
+ * ssd_chunked_fwd — Mamba-2 SSD forward.
+ *
+ * "Accelerating Mamba-2 with high-performance forward kernels in NVIDIA CUDA
+ * Tile": per (batch, head), with a_t = A[h] * dt[t, h] (< 0) and state
+ * h_t of size P x N,
+ *   h_t = exp(a_t) h_{t-1} + x_t b_t^T,   y_t = h_t c_t,
+ * evaluated chunk by chunk with the page's three kernels: the per-chunk
+ * cumulative sum of a_t scaled by log2(e); fwd_pass_state, a sequential loop
+ * over chunks that gives every chunk's initial state and the final state;
+ * and the chunk outputs (C B^T weighted by exp(g_i - g_j) under the causal
+ * mask, times X, plus the initial state's contribution).  x enters the
+ * recurrence as given (pass x * dt for Mamba-2's discretised input).
+ *
+ *  x        [batch, L, H, P] bf16;  dt [batch, L, H] fp32 (> 0);  A [H] fp32 (< 0)
+ *  B, C     [batch, L, G, N] bf16; head h uses group h / (H / G)
+ *  h0       [batch, H, P, N] fp32 initial state, or NULL for zero
+ *  y        [batch, L, H, P] bf16 (written)
+ *  h_final  [batch, H, P, N] fp32 (written): the state after the last token
+ *  workspace >= ssd_workspace_size(batch, L, H, N, chunk) bytes, 16-byte
+ *           aligned; contents on entry are ignored
+ *  P must be 64; N 64 or 128; chunk 64, 128 or 256; H % G == 0.  bf16 and
+ *  state pointers 16-byte aligned, dt and A 4-byte aligned.
+ *  batch == 0 or L == 0 is an empty problem: ATTN_OK, nothing launched.
+ *  Launches three kernels in stream order.  Deterministic.
+ */
+attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, const void* B,
+                              const void* C, const float* h0, void* y, float* h_final, int batch,
+                              int L, int H, int G, int P, int N, int chunk, void* workspace,
+                              size_t workspace_bytes, void* stream);
 
 /*
  * attn_get_device_status — synchronises `stream`, copies the current

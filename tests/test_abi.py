@@ -24,7 +24,7 @@ FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced on these paths
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b((?:attn|fused)_[a-z_0-9]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:attn|fused|ssd)_[a-z_0-9]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")
@@ -117,6 +117,23 @@ def test_fusion_host_validation(lib):
     assert lib.fused_swiglu(FAKE, ctypes.c_void_p(0x10040), 4, 16, None) == INVALID              # out inside gate_up
     assert lib.fused_swiglu(ctypes.c_void_p(0x10008), ctypes.c_void_p(0x40000), 4, 16, None) == INVALID
     assert lib.fused_swiglu(FAKE, FAKE, 0, 16, None) == OK
+
+
+def _ssd(lib, batch=2, L=100, H=8, G=1, P=64, N=128, chunk=64, ws_bytes=None):
+    need = lib.ssd_workspace_size(batch, L, H, N, chunk)
+    return lib.ssd_chunked_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, batch, L, H, G, P, N,
+                               chunk, FAKE, need if ws_bytes is None else ws_bytes, None)
+
+
+def test_ssd_host_validation(lib):
+    assert _ssd(lib, P=128) == UNSUPPORTED
+    assert _ssd(lib, N=96) == UNSUPPORTED
+    assert _ssd(lib, chunk=100) == UNSUPPORTED
+    assert _ssd(lib, H=6, G=4) == INVALID
+    assert _ssd(lib, ws_bytes=16) == WORKSPACE
+    assert _ssd(lib, L=0) == OK
+    # decays (batch*H*n_chunks*chunk fp32, padded to 256 bytes) + initial states
+    assert lib.ssd_workspace_size(2, 100, 8, 128, 64) == 2 * 8 * 2 * 64 * 4 + 2 * 2 * 8 * 64 * 128 * 4
 
 
 def test_workspace_size_formula(lib):
