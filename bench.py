@@ -391,6 +391,13 @@ def paged_prefill_measurement(attn, device, steps, peak):
             "kernels": "kv append + attention (paged mode)", "gpu_launches_per_call": 2}
 
 
+def fusion_bytes(rows, hidden, F):
+    """Algorithmic bytes of one call: add + RMSNorm reads x and residual and
+    writes residual and out (plus the weight once); SwiGLU reads [rows, 2F]
+    and writes [rows, F]; bf16 throughout."""
+    return {"add_rmsnorm": 4 * rows * hidden * 2 + hidden * 2, "swiglu": 3 * rows * F * 2}
+
+
 def fusion_measurement(attn, device, steps, peak_gbs):
     """fused_add_rmsnorm and fused_swiglu on one Qwen2.5-1.5B-sized layer over
     the 16384 prefill tokens (hidden 1536, intermediate 8960), CUDA events over
@@ -403,7 +410,7 @@ def fusion_measurement(attn, device, steps, peak_gbs):
     for i in range(2):
         x, res, w = workloads.add_rmsnorm_inputs(c["rows"], c["hidden"], c["seed"] + 100 * i)
         sets.append((x.to(device), res.to(device), w.to(device), torch.empty_like(x, device=device)))
-    nbytes = 4 * c["rows"] * c["hidden"] * 2 + c["hidden"] * 2
+    nbytes = fusion_bytes(c["rows"], c["hidden"], 0)["add_rmsnorm"]
     stream = torch.cuda.current_stream()
 
     def timed(fn, n):
@@ -425,7 +432,7 @@ def fusion_measurement(attn, device, steps, peak_gbs):
     g = workloads.FUSION_CONFIGS["qwen_swiglu"]
     gu = workloads.swiglu_inputs(g["rows"], g["F"], g["seed"]).to(device)
     out = torch.empty((g["rows"], g["F"]), dtype=torch.bfloat16, device=device)
-    gbytes = 3 * g["rows"] * g["F"] * 2
+    gbytes = fusion_bytes(g["rows"], 0, g["F"])["swiglu"]
     ms_glu = timed(lambda i: attn.fused_swiglu(gu, out=out), steps)
     del gu, out
     res = {}
