@@ -53,11 +53,11 @@ NSETS = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
 # ncu summaries (profiles/), taken on this workload; None once a kernel changes
-# until it is captured again.  Forward: medians over the 10 launches of the
-# bench step in one capture (reads are q + k + v; writes vary with what o and
-# lse leave in L2).  Decode: main kernel + merge kernel.
+# until it is captured again.  Medians over the 10 bench-step launches of one
+# capture (launches_all_bench_workloads.md).  Forward: reads are q + k + v;
+# writes vary with what o and lse leave in L2.  Decode: main kernel + merge.
 TRAFFIC_FWD = 67192448 + 4752640
-TRAFFIC_DEC = (132292096 + 3670272) + (3272704 + 0)
+TRAFFIC_DEC = (132293888 + 192384) + (3272192 + 0)
 
 
 def peaks():
