@@ -587,7 +587,8 @@ attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, co
   if ((reinterpret_cast<uintptr_t>(dt) & 3u) || (reinterpret_cast<uintptr_t>(A) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "dt and A must be 4-byte aligned");
   const long long nc = (static_cast<long long>(L) + chunk - 1) / chunk;
-  if (static_cast<long long>(batch) * nc * H * (chunk / 64) > 0x7fffffffLL)
+  if (static_cast<long long>(batch) * nc * H * (chunk / 64) > 0x7fffffffLL ||
+      static_cast<long long>(batch) * H * (N / 64) > 0x7fffffffLL)
     return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
   const size_t need = ssd_workspace_size(batch, L, H, N, chunk);
   if (workspace_bytes < need)

@@ -365,7 +365,7 @@ cudaError_t launch_ssd_sm103(const SsdLaunch& a) {
   const int smem2 = 2 * (StateSmem::x_bytes(a.chunk) + StateSmem::b_bytes(a.chunk) + a.chunk * 4);
   e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
   if (e != cudaSuccess) return e;
-  const unsigned grid2 = static_cast<unsigned>(a.batch * a.H * (a.N / kNT));
+  const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(a.batch) * a.H * (a.N / kNT));
   ssd_state_kernel<<<grid2, kThreads, smem2, a.stream>>>(
       static_cast<const uint8_t*>(a.x), static_cast<const uint8_t*>(a.B), g, a.h0, s_init, a.h_final,
       a.L, a.H, a.G, a.N, nc, a.chunk);
