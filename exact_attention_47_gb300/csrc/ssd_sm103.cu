@@ -6,7 +6,8 @@
 //      by log2(e) so that every later exponential is an exp2;
 //   2. ssd_state_kernel (fwd_pass_state): one CTA per (batch, head, 64-wide
 //      state tile) walks the chunks in order, storing each chunk's initial
-//      state and carrying it across the chunk with the jump formula
+//      state (in bf16: the output kernel's matrix product takes it in bf16)
+//      and carrying it across the chunk in fp32 with the jump formula
 //        S <- 2^(g_last) S + sum_j 2^(g_last - g_j) x_j b_j^T
 //      (the sum is a (P x Q) * (Q x 64) contraction on the tensor cores);
 //   3. ssd_out_kernel: one CTA per (batch, chunk, head, 64-row block) forms
@@ -88,7 +89,7 @@ struct StateSmem {
 __global__ void __launch_bounds__(kThreads)
     ssd_state_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ Bm,
                      const float* __restrict__ g, const float* __restrict__ h0,
-                     float* __restrict__ s_init, float* __restrict__ h_final, int L, int H, int G,
+                     uint8_t* __restrict__ s_init, float* __restrict__ h_final, int L, int H, int G,
                      int N, int nc, int Q) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,15 +160,16 @@ __global__ void __launch_bounds__(kThreads)
         vw[k] = pack_bf16x2(__uint_as_float(vw[k] << 16) * w, __uint_as_float(vw[k] & 0xffff0000u) * w);
       *piece = v;
     }
-    // Store this chunk's initial state, then decay it to the chunk's end.
+    // Store this chunk's initial state (bf16), then decay it to the chunk's end.
     const float decay = exp2f(g_last);
-    float* si = s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N;
+    uint8_t* si = s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N * 2;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int p = pr + 8 * e2, n = n0 + 8 * j + nc2;
-        *reinterpret_cast<float2*>(si + static_cast<size_t>(p) * N + n) = make_float2(S[j][2 * e2], S[j][2 * e2 + 1]);
+        *reinterpret_cast<uint32_t*>(si + (static_cast<size_t>(p) * N + n) * 2) =
+            pack_bf16x2(S[j][2 * e2], S[j][2 * e2 + 1]);
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) S[j][e] *= decay;
@@ -211,7 +213,7 @@ template <int N>
 __global__ void __launch_bounds__(kThreads)
     ssd_out_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ Bm,
                    const uint8_t* __restrict__ Cm, const float* __restrict__ g,
-                   const float* __restrict__ s_init, uint8_t* __restrict__ y, int L, int H, int G,
+                   const uint8_t* __restrict__ s_init, uint8_t* __restrict__ y, int L, int H, int G,
                    int nc, int Q) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,20 +241,13 @@ __global__ void __launch_bounds__(kThreads)
   load_tile(sB, Bm + ((static_cast<size_t>(b) * L + t0) * G + grp) * N * 2, bc_row, jrows, N, n_len);
   load_tile(sX, x + ((static_cast<size_t>(b) * L + t0) * H + h) * kP * 2, static_cast<size_t>(H) * kP * 2,
             jrows, kP, n_len);
+  // The chunk's initial state S [p][n] (bf16, as the state kernel stored it).
+  load_tile(sS, s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N * 2,
+            static_cast<size_t>(N) * 2, kP, N, kP);
   const float* g_c = g + ((static_cast<size_t>(b) * H + h) * nc + c) * Q;
   for (int i = threadIdx.x; i < Q / 4; i += kThreads) cp_async16(smem_addr(gs) + i * 16, g_c + i * 4, 16u);
   cp_async_commit();
-  // The chunk's initial state, fp32 -> bf16, as S [p][n].
-  const float* si = s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N;
-  for (int i = threadIdx.x; i < kP * (N / 8); i += kThreads) {
-    const int p = i / (N / 8), c8 = i % (N / 8);
-    const float4 lo = __ldg(reinterpret_cast<const float4*>(si + static_cast<size_t>(p) * N + c8 * 8));
-    const float4 hi = __ldg(reinterpret_cast<const float4*>(si + static_cast<size_t>(p) * N + c8 * 8 + 4));
-    *reinterpret_cast<uint4*>(smem + (sS - s0) + swz(kP, p, c8)) =
-        make_uint4(pack_bf16x2(lo.x, lo.y), pack_bf16x2(lo.z, lo.w), pack_bf16x2(hi.x, hi.y), pack_bf16x2(hi.z, hi.w));
-  }
   cp_async_wait<0>();
-  fence_proxy_async_smem();
   __syncthreads();
 
   // Rows of this warp: i = ib*64 + 16*warp + lane/4 (+8); A fragments of C_i
@@ -344,7 +339,7 @@ __global__ void __launch_bounds__(kThreads)
 size_t ssd_workspace_bytes(int batch, int L, int H, int N, int chunk) {
   const size_t nc = (static_cast<size_t>(L) + chunk - 1) / chunk;
   const size_t g_bytes = static_cast<size_t>(batch) * H * nc * chunk * 4;
-  const size_t s_bytes = static_cast<size_t>(batch) * nc * H * kP * N * 4;
+  const size_t s_bytes = static_cast<size_t>(batch) * nc * H * kP * N * 2;
   return ((g_bytes + 255) & ~static_cast<size_t>(255)) + s_bytes;
 }
 
@@ -354,8 +349,7 @@ cudaError_t launch_ssd_sm103(const SsdLaunch& a) {
   const int nc = (a.L + a.chunk - 1) / a.chunk;
   const size_t g_bytes = static_cast<size_t>(a.batch) * a.H * nc * a.chunk * 4;
   float* g = static_cast<float*>(a.workspace);
-  float* s_init = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
-                                           ((g_bytes + 255) & ~static_cast<size_t>(255)));
+  uint8_t* s_init = static_cast<uint8_t*>(a.workspace) + ((g_bytes + 255) & ~static_cast<size_t>(255));
   const long long n1 = static_cast<long long>(a.batch) * nc * a.H;
   ssd_cumsum_kernel<<<static_cast<unsigned>((n1 + kThreads - 1) / kThreads), kThreads, 0, a.stream>>>(
       a.dt, a.A, g, a.batch, a.L, a.H, nc, a.chunk);

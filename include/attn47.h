@@ -317,9 +317,9 @@ attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void
 
 /*
  * ssd_workspace_size — bytes of device workspace ssd_chunked_fwd needs: the
- * per-chunk cumulative decays (fp32, batch * H * n_chunks * chunk) and every
- * chunk's initial state (fp32, batch * n_chunks * H * 64 * N).  0 for an
- * empty problem.
+ * per-chunk cumulative decays (fp32, batch * H * n_chunks * chunk, padded to
+ * 256 bytes) and every chunk's initial state (bf16, batch * n_chunks * H *
+ * 64 * N).  0 for an empty problem.
  */
 size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk);
 

@@ -132,8 +132,8 @@ def test_ssd_host_validation(lib):
     assert _ssd(lib, H=6, G=4) == INVALID
     assert _ssd(lib, ws_bytes=16) == WORKSPACE
     assert _ssd(lib, L=0) == OK
-    # decays (batch*H*n_chunks*chunk fp32, padded to 256 bytes) + initial states
-    assert lib.ssd_workspace_size(2, 100, 8, 128, 64) == 2 * 8 * 2 * 64 * 4 + 2 * 2 * 8 * 64 * 128 * 4
+    # decays (batch*H*n_chunks*chunk fp32, padded to 256 bytes) + initial states (bf16)
+    assert lib.ssd_workspace_size(2, 100, 8, 128, 64) == 2 * 8 * 2 * 64 * 4 + 2 * 2 * 8 * 64 * 128 * 2
 
 
 def test_workspace_size_formula(lib):
