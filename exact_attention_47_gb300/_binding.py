@@ -93,9 +93,13 @@ def _check(func, status):
         raise AttnError(func, status, load_library().attn_last_error().decode())
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
+    """The raw cudaStream_t of `stream` (default: torch's current stream of
+    `device`); a stream of another device is refused."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != device:
+        raise ValueError("stream is on %s but the tensors are on %s" % (stream.device, device))
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -103,15 +107,53 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _need_cuda(name, t, dtype):
+def _need_cuda(name, t, dtype, device=None):
+    """`t` is a contiguous CUDA tensor of `dtype` (any dtype if None) on
+    `device` (if given)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dtype != dtype:
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the other tensors on %s" % (name, t.device, device))
+    if dtype is not None and t.dtype != dtype:
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+
+
+def _need_shape(name, t, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _output(name, t, shape, dtype, device):
+    """A caller-given output checked for device, dtype and shape, or a new one."""
+    if t is None:
+        return torch.empty(tuple(shape), dtype=dtype, device=device)
+    _need_cuda(name, t, dtype, device)
+    _need_shape(name, t, shape)
+    return t
+
+
+def _workspace(name, t, need, device):
+    """A caller-given workspace (any dtype, contiguous, on `device`, at least
+    `need` bytes), or a new one of `need` bytes."""
+    if t is None:
+        return torch.empty(max(int(need), 16), dtype=torch.uint8, device=device)
+    _need_cuda(name, t, None, device)
+    nbytes = t.numel() * t.element_size()
+    if nbytes < need:
+        raise ValueError("%s has %d bytes, needs %d" % (name, nbytes, need))
+    return t
+
+
+def _call(func, device, *args):
+    """Call C entry point `func` with `device` current and raise on error."""
+    lib = load_library()
+    with torch.cuda.device(device):
+        st = getattr(lib, func)(*args)
+    _check(func, st)
 
 
 def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None, return_lse=True, stream=None):
@@ -120,9 +162,10 @@ def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None, return_lse=True
     Returns (o, lse): o [B,Hq,N,d] bf16, lse [B,Hq,N] fp32 (None when
     ``return_lse`` is False and no ``lse`` buffer is given).
     """
-    lib = load_library()
+    _need_cuda("q", q, torch.bfloat16)
+    dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _need_cuda(name, t, torch.bfloat16)
+        _need_cuda(name, t, torch.bfloat16, dev)
         if t.dim() != 4:
             raise ValueError("%s must be 4-D [B, H, N, d]" % name)
     B, Hq, N, d = q.shape
@@ -131,21 +174,11 @@ def attn_fwd(q, k, v, causal=True, scale=None, o=None, lse=None, return_lse=True
     Hkv = k.shape[1]
     if scale is None:
         scale = d ** -0.5
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _need_cuda("o", o, torch.bfloat16)
-        if o.shape != q.shape:
-            raise ValueError("o must have q's shape")
-    if lse is None and return_lse:
-        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    elif lse is not None:
-        _need_cuda("lse", lse, torch.float32)
-        if tuple(lse.shape) != (B, Hq, N):
-            raise ValueError("lse must be [B, Hq, N]")
-    st = lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
-                      1 if causal else 0, float(scale), _stream_handle(stream))
-    _check("attn_fwd", st)
+    o = _output("o", o, q.shape, torch.bfloat16, dev)
+    if lse is not None or return_lse:
+        lse = _output("lse", lse, (B, Hq, N), torch.float32, dev)
+    _call("attn_fwd", dev, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+          1 if causal else 0, float(scale), _stream_handle(stream, dev))
     return o, lse
 
 
@@ -160,39 +193,59 @@ def attn_bwd(q, k, v, o, lse, dout, causal=True, scale=None, dq=None, dk=None, d
 
     Returns (dq [B,Hq,N,d], dk [B,Hkv,N,d], dv [B,Hkv,N,d]) bf16.
     """
-    lib = load_library()
+    _need_cuda("q", q, torch.bfloat16)
+    dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
-        _need_cuda(name, t, torch.bfloat16)
+        _need_cuda(name, t, torch.bfloat16, dev)
         if t.dim() != 4:
             raise ValueError("%s must be 4-D [B, H, N, d]" % name)
-    _need_cuda("lse", lse, torch.float32)
+    _need_cuda("lse", lse, torch.float32, dev)
     B, Hq, N, d = q.shape
     if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d or v.shape != k.shape:
         raise ValueError("k and v must be [B, Hkv, N, d] matching q")
-    if o.shape != q.shape or dout.shape != q.shape or tuple(lse.shape) != (B, Hq, N):
-        raise ValueError("o and dout must have q's shape, lse [B, Hq, N]")
+    _need_shape("o", o, q.shape)
+    _need_shape("dout", dout, q.shape)
+    _need_shape("lse", lse, (B, Hq, N))
     Hkv = k.shape[1]
     if scale is None:
         scale = d ** -0.5
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    for name, t, ref in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
-        _need_cuda(name, t, torch.bfloat16)
-        if t.shape != ref.shape:
-            raise ValueError("%s has the wrong shape" % name)
-    need = attn_bwd_workspace_size(B, Hq, N)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
-                      _ptr(dv), B, Hq, Hkv, N, d, 1 if causal else 0, float(scale), _ptr(workspace),
-                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
-    _check("attn_bwd", st)
+    dq = _output("dq", dq, q.shape, torch.bfloat16, dev)
+    dk = _output("dk", dk, k.shape, torch.bfloat16, dev)
+    dv = _output("dv", dv, v.shape, torch.bfloat16, dev)
+    workspace = _workspace("workspace", workspace, attn_bwd_workspace_size(B, Hq, N), dev)
+    _call("attn_bwd", dev, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+          _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, 1 if causal else 0, float(scale), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     return dq, dk, dv
 
 
 def attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq):
     return int(load_library().attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq))
+
+
+def _decode_args(q, k_cache, v_cache, block_table, seq_lens, scale, o, lse, return_lse):
+    """Checks shared by both decode entry points; returns the sizes, the
+    scale and the (checked or new) outputs."""
+    _need_cuda("q", q, torch.bfloat16)
+    dev = q.device
+    for name, t, dt in (("k_cache", k_cache, torch.bfloat16), ("v_cache", v_cache, torch.bfloat16),
+                        ("block_table", block_table, torch.int32), ("seq_lens", seq_lens, torch.int32)):
+        _need_cuda(name, t, dt, dev)
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [S,Hq,d] and caches [num_blocks,Hkv,block_size,d]")
+    S, Hq, d = q.shape
+    num_blocks, Hkv, block_size, dc = k_cache.shape
+    if dc != d:
+        raise ValueError("cache head dim %d differs from q's %d" % (dc, d))
+    if block_table.dim() != 2 or block_table.shape[0] != S:
+        raise ValueError("block_table must be [S, max_blocks]")
+    _need_shape("seq_lens", seq_lens, (S,))
+    o = _output("o", o, (S, Hq, d), torch.bfloat16, dev)
+    if lse is not None or return_lse:
+        lse = _output("lse", lse, (S, Hq), torch.float32, dev)
+    if scale is None:
+        scale = d ** -0.5
+    return dev, S, Hq, Hkv, d, block_size, block_table.shape[1], num_blocks, float(scale), o, lse
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, o=None, lse=None,
@@ -202,37 +255,12 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale=None, o=
 
     Returns (o [S,Hq,d] bf16, lse [S,Hq] fp32 or None).
     """
-    lib = load_library()
-    _need_cuda("q", q, torch.bfloat16)
-    _need_cuda("k_cache", k_cache, torch.bfloat16)
-    _need_cuda("v_cache", v_cache, torch.bfloat16)
-    _need_cuda("block_table", block_table, torch.int32)
-    _need_cuda("seq_lens", seq_lens, torch.int32)
-    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("q must be [S,Hq,d] and caches [num_blocks,Hkv,block_size,d]")
-    S, Hq, d = q.shape
-    num_blocks, Hkv, block_size, dk = k_cache.shape
-    if dk != d:
-        raise ValueError("cache head dim differs from q")
-    if block_table.dim() != 2 or block_table.shape[0] != S or tuple(seq_lens.shape) != (S,):
-        raise ValueError("block_table must be [S, max_blocks] and seq_lens [S]")
-    max_blocks = block_table.shape[1]
-    if scale is None:
-        scale = d ** -0.5
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _need_cuda("o", o, torch.bfloat16)
-    if lse is None and return_lse:
-        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
-    need = attn_decode_paged_workspace_size(S, Hq, d, max_blocks)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = lib.attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                               _ptr(seq_lens), S, Hq, Hkv, d, block_size, max_blocks, num_blocks,
-                               float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream_handle(stream))
-    _check("attn_decode_paged", st)
+    dev, S, Hq, Hkv, d, bs, mb, nb, scale, o, lse = _decode_args(
+        q, k_cache, v_cache, block_table, seq_lens, scale, o, lse, return_lse)
+    workspace = _workspace("workspace", workspace, attn_decode_paged_workspace_size(S, Hq, d, mb), dev)
+    _call("attn_decode_paged", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+          _ptr(seq_lens), S, Hq, Hkv, d, bs, mb, nb, scale, _ptr(o), _ptr(lse), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     return o, lse
 
 
@@ -245,28 +273,11 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale=
     that array and must be ordered.  Only the outputs, if not given, are
     allocated here, by torch; pass ``o`` (and ``lse`` or return_lse=False)
     to allocate nothing at all."""
-    lib = load_library()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
-                        ("v_cache", v_cache, torch.bfloat16), ("block_table", block_table, torch.int32),
-                        ("seq_lens", seq_lens, torch.int32)):
-        _need_cuda(name, t, dt)
-    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
-        raise ValueError("q must be [S,Hq,d] and caches [num_blocks,Hkv,block_size,d]")
-    S, Hq, d = q.shape
-    num_blocks, Hkv, block_size, _ = k_cache.shape
-    if scale is None:
-        scale = d ** -0.5
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _need_cuda("o", o, torch.bfloat16)
-    if lse is None and return_lse:
-        lse = torch.empty((S, Hq), dtype=torch.float32, device=q.device)
-    st = lib.attn_decode_paged_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
-                                       _ptr(seq_lens), S, Hq, Hkv, d, block_size,
-                                       block_table.shape[1], num_blocks, float(scale), _ptr(o),
-                                       _ptr(lse), _stream_handle(stream))
-    _check("attn_decode_paged_noalloc", st)
+    dev, S, Hq, Hkv, d, bs, mb, nb, scale, o, lse = _decode_args(
+        q, k_cache, v_cache, block_table, seq_lens, scale, o, lse, return_lse)
+    _call("attn_decode_paged_noalloc", dev, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+          _ptr(seq_lens), S, Hq, Hkv, d, bs, mb, nb, scale, _ptr(o), _ptr(lse),
+          _stream_handle(stream, dev))
     return o, lse
 
 
@@ -280,12 +291,12 @@ def attn_prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens,
     int32 (left unchanged).  Returns (o [S,Hq,N,d] bf16, lse [S,Hq,N] fp32 or
     None).
     """
-    lib = load_library()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k_new", k_new, torch.bfloat16),
-                        ("v_new", v_new, torch.bfloat16), ("k_cache", k_cache, torch.bfloat16),
-                        ("v_cache", v_cache, torch.bfloat16), ("block_table", block_table, torch.int32),
-                        ("ctx_lens", ctx_lens, torch.int32)):
-        _need_cuda(name, t, dt)
+    _need_cuda("q", q, torch.bfloat16)
+    dev = q.device
+    for name, t, dt in (("k_new", k_new, torch.bfloat16), ("v_new", v_new, torch.bfloat16),
+                        ("k_cache", k_cache, torch.bfloat16), ("v_cache", v_cache, torch.bfloat16),
+                        ("block_table", block_table, torch.int32), ("ctx_lens", ctx_lens, torch.int32)):
+        _need_cuda(name, t, dt, dev)
     if q.dim() != 4 or k_new.dim() != 4 or k_new.shape != v_new.shape:
         raise ValueError("q must be [S,Hq,N,d] and k_new / v_new [S,Hkv,N,d]")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
@@ -294,27 +305,17 @@ def attn_prefill_paged(q, k_new, v_new, k_cache, v_cache, block_table, ctx_lens,
     num_blocks, Hkv, block_size, dc = k_cache.shape
     if k_new.shape != (S, Hkv, N, d) or dc != d:
         raise ValueError("k_new / v_new must be [S, Hkv, N, d] matching q and the caches")
-    if block_table.dim() != 2 or block_table.shape[0] != S or tuple(ctx_lens.shape) != (S,):
-        raise ValueError("block_table must be [S, max_blocks] and ctx_lens [S]")
+    if block_table.dim() != 2 or block_table.shape[0] != S:
+        raise ValueError("block_table must be [S, max_blocks]")
+    _need_shape("ctx_lens", ctx_lens, (S,))
     if scale is None:
         scale = d ** -0.5
-    if o is None:
-        o = torch.empty_like(q)
-    else:
-        _need_cuda("o", o, torch.bfloat16)
-        if o.shape != q.shape:
-            raise ValueError("o must have q's shape")
-    if lse is None and return_lse:
-        lse = torch.empty((S, Hq, N), dtype=torch.float32, device=q.device)
-    elif lse is not None:
-        _need_cuda("lse", lse, torch.float32)
-        if tuple(lse.shape) != (S, Hq, N):
-            raise ValueError("lse must be [S, Hq, N]")
-    st = lib.attn_prefill_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                _ptr(block_table), _ptr(ctx_lens), S, Hq, Hkv, N, d, block_size,
-                                block_table.shape[1], num_blocks, float(scale), _ptr(o), _ptr(lse),
-                                _stream_handle(stream))
-    _check("attn_prefill_paged", st)
+    o = _output("o", o, q.shape, torch.bfloat16, dev)
+    if lse is not None or return_lse:
+        lse = _output("lse", lse, (S, Hq, N), torch.float32, dev)
+    _call("attn_prefill_paged", dev, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+          _ptr(block_table), _ptr(ctx_lens), S, Hq, Hkv, N, d, block_size, block_table.shape[1],
+          num_blocks, float(scale), _ptr(o), _ptr(lse), _stream_handle(stream, dev))
     return o, lse
 
 
@@ -322,40 +323,29 @@ def fused_add_rmsnorm(x, residual, weight, eps=1e-6, out=None, stream=None):
     """Residual add + RMSNorm.  x, residual [rows, hidden] and weight [hidden]
     bf16 on the GPU; ``residual`` is overwritten with bf16(x + residual).
     Returns (out [rows, hidden] bf16, residual)."""
-    lib = load_library()
-    for name, t in (("x", x), ("residual", residual), ("weight", weight)):
-        _need_cuda(name, t, torch.bfloat16)
+    _need_cuda("x", x, torch.bfloat16)
+    dev = x.device
+    for name, t in (("residual", residual), ("weight", weight)):
+        _need_cuda(name, t, torch.bfloat16, dev)
     if x.dim() != 2 or residual.shape != x.shape or weight.dim() != 1 or weight.shape[0] != x.shape[1]:
         raise ValueError("x and residual must be [rows, hidden] and weight [hidden]")
     rows, hidden = x.shape
-    if out is None:
-        out = torch.empty_like(x)
-    else:
-        _need_cuda("out", out, torch.bfloat16)
-        if out.shape != x.shape:
-            raise ValueError("out must have x's shape")
-    st = lib.fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), _ptr(out), rows, hidden,
-                               float(eps), _stream_handle(stream))
-    _check("fused_add_rmsnorm", st)
+    out = _output("out", out, x.shape, torch.bfloat16, dev)
+    _call("fused_add_rmsnorm", dev, _ptr(x), _ptr(residual), _ptr(weight), _ptr(out), rows, hidden,
+          float(eps), _stream_handle(stream, dev))
     return out, residual
 
 
 def fused_swiglu(gate_up, out=None, stream=None):
     """SwiGLU activation of the merged gate/up projection output
     gate_up [rows, 2F] bf16 (gate first): returns silu(gate) * up [rows, F] bf16."""
-    lib = load_library()
     _need_cuda("gate_up", gate_up, torch.bfloat16)
+    dev = gate_up.device
     if gate_up.dim() != 2 or gate_up.shape[1] % 2 != 0:
         raise ValueError("gate_up must be [rows, 2F]")
     rows, F = gate_up.shape[0], gate_up.shape[1] // 2
-    if out is None:
-        out = torch.empty((rows, F), dtype=torch.bfloat16, device=gate_up.device)
-    else:
-        _need_cuda("out", out, torch.bfloat16)
-        if tuple(out.shape) != (rows, F):
-            raise ValueError("out must be [rows, F]")
-    st = lib.fused_swiglu(_ptr(gate_up), _ptr(out), rows, F, _stream_handle(stream))
-    _check("fused_swiglu", st)
+    out = _output("out", out, (rows, F), torch.bfloat16, dev)
+    _call("fused_swiglu", dev, _ptr(gate_up), _ptr(out), rows, F, _stream_handle(stream, dev))
     return out
 
 
@@ -369,10 +359,11 @@ def ssd_chunked_fwd(x, dt, A, B, C, chunk=256, h0=None, y=None, h_final=None, wo
     A [H] fp32, B and C [batch, L, G, N] bf16, h0 [batch, H, P, N] fp32 or
     None, all on the GPU.  Returns (y [batch, L, H, P] bf16, h_final
     [batch, H, P, N] fp32)."""
-    lib = load_library()
-    for name, t, dtype in (("x", x, torch.bfloat16), ("dt", dt, torch.float32), ("A", A, torch.float32),
+    _need_cuda("x", x, torch.bfloat16)
+    dev = x.device
+    for name, t, dtype in (("dt", dt, torch.float32), ("A", A, torch.float32),
                            ("B", B, torch.bfloat16), ("C", C, torch.bfloat16)):
-        _need_cuda(name, t, dtype)
+        _need_cuda(name, t, dtype, dev)
     if x.dim() != 4 or dt.dim() != 3 or A.dim() != 1 or B.dim() != 4 or C.shape != B.shape:
         raise ValueError("x [batch, L, H, P], dt [batch, L, H], A [H], B/C [batch, L, G, N]")
     batch, L, H, P = x.shape
@@ -380,20 +371,14 @@ def ssd_chunked_fwd(x, dt, A, B, C, chunk=256, h0=None, y=None, h_final=None, wo
     if tuple(dt.shape) != (batch, L, H) or A.shape[0] != H or B.shape[:2] != x.shape[:2]:
         raise ValueError("dt, A, B and C do not match x")
     if h0 is not None:
-        _need_cuda("h0", h0, torch.float32)
-        if tuple(h0.shape) != (batch, H, P, N):
-            raise ValueError("h0 must be [batch, H, P, N]")
-    y = torch.empty_like(x) if y is None else y
-    h_final = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device) if h_final is None else h_final
-    _need_cuda("y", y, torch.bfloat16)
-    _need_cuda("h_final", h_final, torch.float32)
-    need = ssd_workspace_size(batch, L, H, N, chunk)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
-    st = lib.ssd_chunked_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(y), _ptr(h_final),
-                             batch, L, H, G, P, N, chunk, _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
-    _check("ssd_chunked_fwd", st)
+        _need_cuda("h0", h0, torch.float32, dev)
+        _need_shape("h0", h0, (batch, H, P, N))
+    y = _output("y", y, x.shape, torch.bfloat16, dev)
+    h_final = _output("h_final", h_final, (batch, H, P, N), torch.float32, dev)
+    workspace = _workspace("workspace", workspace, ssd_workspace_size(batch, L, H, N, chunk), dev)
+    _call("ssd_chunked_fwd", dev, _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0), _ptr(y),
+          _ptr(h_final), batch, L, H, G, P, N, chunk, _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     return y, h_final
 
 

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "attn47.h"
@@ -45,6 +46,7 @@ int g_decode_max_ctas = 0;  // 0 = one full wave
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
+  int index = -1;
   bool checked = false;
   bool usable = false;
   int sms = 0;
@@ -59,6 +61,8 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+using AddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+AddressRangeFn g_address_range = nullptr;
 
 // Current device, checked once: compute capability 10.3, status word address.
 attn_status_t current_device(DeviceInfo** out) {
@@ -75,6 +79,7 @@ attn_status_t current_device(DeviceInfo** out) {
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     d.sms = sms;
+    d.index = dev;
     if (major != 10 || minor != 3) {
       d.checked = true;
       d.usable = false;
@@ -94,6 +99,15 @@ attn_status_t current_device(DeviceInfo** out) {
         return fail(ATTN_ERR_DEVICE, "driver entry point cuTensorMapEncodeTiled not found");
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
+    if (g_address_range == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000, cudaEnableDefault, &q);
+      if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn != nullptr)
+        g_address_range = reinterpret_cast<AddressRangeFn>(fn);
+      else
+        cudaGetLastError();   // optional: without it only the memory type is checked
+    }
     d.usable = true;
     d.checked = true;
   }
@@ -108,6 +122,49 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
+
+// A buffer a kernel will read or write: `bytes` from `p` (p may be NULL when
+// the argument is optional).
+struct Buf {
+  const void* p;
+  size_t bytes;
+  const char* name;
+};
+
+// Every buffer must be memory the current device owns (cudaMalloc'd, from a
+// stream-ordered pool, or managed), and [p, p + bytes) must lie inside the
+// allocation that holds p.  A host address (pageable or pinned) handed to
+// TMA or to a kernel would be accessed as if it were device memory, and an
+// undersized buffer would be overrun; both are refused here, before any
+// launch, with ATTN_ERR_INVALID_ARG.
+attn_status_t check_bufs(const DeviceInfo& d, std::initializer_list<Buf> bufs) {
+  for (const Buf& b : bufs) {
+    if (b.p == nullptr || b.bytes == 0) continue;
+    cudaPointerAttributes attr;
+    const cudaError_t e = cudaPointerGetAttributes(&attr, b.p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();   // not a launch error: clear it
+      return fail(ATTN_ERR_INVALID_ARG, "%s (%p) is not device memory: %s", b.name, b.p,
+                  cudaGetErrorString(e));
+    }
+    const bool ok = attr.type == cudaMemoryTypeManaged ||
+                    (attr.type == cudaMemoryTypeDevice && attr.device == d.index);
+    if (!ok)
+      return fail(ATTN_ERR_INVALID_ARG, "%s (%p) is not memory of device %d (memory type %d, device %d)",
+                  b.name, b.p, d.index, (int)attr.type, attr.device);
+    if (g_address_range != nullptr) {
+      CUdeviceptr base = 0;
+      size_t size = 0;
+      if (g_address_range(&base, &size, reinterpret_cast<CUdeviceptr>(b.p)) == CUDA_SUCCESS) {
+        const uintptr_t end = static_cast<uintptr_t>(base) + size;
+        if (reinterpret_cast<uintptr_t>(b.p) + b.bytes > end)
+          return fail(ATTN_ERR_INVALID_ARG, "%s: %zu bytes from %p run past the end of its allocation "
+                      "(%zu bytes at %p)", b.name, b.bytes, b.p, size, reinterpret_cast<void*>(base));
+      }
+    }
+  }
+  return ATTN_OK;
+}
 
 // bf16 tensor map over `rank` dims (innermost first), 64-column boxes,
 // 128-byte swizzle, zero fill out of bounds.
@@ -132,6 +189,95 @@ attn_status_t launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "%s launch failed: %s", what, cudaGetErrorString(e));
   g_last_error[0] = '\0';
   return ATTN_OK;
+}
+
+// Host-side checks of a decode call that need neither the workspace nor the
+// device: sizes, supported shapes, null and misaligned pointers.  Shared by
+// attn_decode_paged and attn_decode_paged_noalloc.
+attn_status_t decode_check_args(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, int num_seqs,
+                                int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
+                                int num_blocks, float scale, const void* o, const float* lse) {
+  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "sizes must satisfy num_seqs >= 0, Hq, Hkv, max_blocks_per_seq, num_blocks >= 1");
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
+  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (block_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
+  if (Hq / Hkv > 16) return fail(ATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16 not supported", Hq / Hkv);
+  if (static_cast<long long>(num_blocks) * Hkv * block_size >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "KV pool too large (num_blocks * Hkv * 16 >= 2^31)");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  if (static_cast<long long>(num_seqs) * Hq >= 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "num_seqs * Hq too large");
+  if (num_seqs == 0) return ATTN_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o)
+    return fail(ATTN_ERR_INVALID_ARG, "q, caches, block_table, seq_lens and o must be non-null");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o))
+    return fail(ATTN_ERR_INVALID_ARG, "q, caches and o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "block_table, seq_lens and lse must be 4-byte aligned");
+  return ATTN_OK;
+}
+
+// Bytes of every decode buffer other than the workspace.
+struct DecodeBytes {
+  size_t q, cache, table, lens, o, lse;
+};
+DecodeBytes decode_bytes(int num_seqs, int Hq, int Hkv, int d, int max_blocks, int num_blocks) {
+  DecodeBytes b;
+  b.q = b.o = static_cast<size_t>(num_seqs) * Hq * d * 2;
+  b.cache = static_cast<size_t>(num_blocks) * Hkv * 16 * d * 2;
+  b.table = static_cast<size_t>(num_seqs) * max_blocks * 4;
+  b.lens = static_cast<size_t>(num_seqs) * 4;
+  b.lse = static_cast<size_t>(num_seqs) * Hq * 4;
+  return b;
+}
+
+// Checks the decode's buffers against the device, encodes the cache maps and
+// launches the decode with a workspace that has already been checked.
+attn_status_t decode_launch(const DeviceInfo& dev, const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                            int num_seqs, int Hq, int Hkv, int d, int max_blocks_per_seq, int num_blocks,
+                            float scale, void* o, float* lse, void* workspace, void* stream) {
+  const DecodeBytes nb = decode_bytes(num_seqs, Hq, Hkv, d, max_blocks_per_seq, num_blocks);
+  attn_status_t st = check_bufs(dev, {{q, nb.q, "q"}, {k_cache, nb.cache, "k_cache"},
+                                      {v_cache, nb.cache, "v_cache"}, {block_table, nb.table, "block_table"},
+                                      {seq_lens, nb.lens, "seq_lens"}, {o, nb.o, "o"}, {lse, nb.lse, "lse"}});
+  if (st != ATTN_OK) return st;
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(num_blocks) * Hkv * 16};
+  alignas(64) CUtensorMap tk, tv;
+  if ((st = encode_bf16(&tk, k_cache, 2, dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16(&tv, v_cache, 2, dims, box)) != ATTN_OK) return st;
+
+  attn47::DecLaunch a;
+  a.tk = &tk;
+  a.tv = &tv;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.o = o;
+  a.lse = lse;
+  a.workspace = static_cast<float*>(workspace);
+  a.num_seqs = num_seqs;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.d = d;
+  a.max_blocks = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.sms = dev.sms;
+  a.max_ctas = g_decode_max_ctas;
+  a.scale = scale;
+  a.status = dev.status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_decode_sm103(a), "attn_decode_paged");
 }
 
 __global__ void selftest_wait_kernel(unsigned int* status, unsigned long long timeout_ns) {
@@ -194,6 +340,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  const size_t qb = static_cast<size_t>(B) * Hq * N * d * 2, kvb = static_cast<size_t>(B) * Hkv * N * d * 2;
+  if ((st = check_bufs(*dev, {{q, qb, "q"}, {k, kvb, "k"}, {v, kvb, "v"}, {o, qb, "o"},
+                              {lse, static_cast<size_t>(B) * Hq * N * 4, "lse"}})) != ATTN_OK)
+    return st;
 
   const cuuint32_t rows = static_cast<cuuint32_t>(attn47::fwd_box_rows());
   const cuuint32_t box[3] = {64, rows, 1};
@@ -262,6 +412,12 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  const size_t qb = static_cast<size_t>(B) * Hq * N * d * 2, kvb = static_cast<size_t>(B) * Hkv * N * d * 2;
+  if ((st = check_bufs(*dev, {{q, qb, "q"}, {k, kvb, "k"}, {v, kvb, "v"}, {o, qb, "o"},
+                              {lse, static_cast<size_t>(B) * Hq * N * 4, "lse"}, {dout, qb, "dout"},
+                              {dq, qb, "dq"}, {dk, kvb, "dk"}, {dv, kvb, "dv"},
+                              {workspace, need, "workspace"}})) != ATTN_OK)
+    return st;
 
   const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(attn47::bwd_box_rows()), 1};
   const cuuint64_t dq_dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -309,67 +465,32 @@ attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* 
                                 int Hq, int Hkv, int d, int block_size, int max_blocks_per_seq,
                                 int num_blocks, float scale, void* o, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream) {
-  if (num_seqs < 0 || Hq < 1 || Hkv < 1 || max_blocks_per_seq < 1 || num_blocks < 1)
-    return fail(ATTN_ERR_INVALID_ARG,
-                "sizes must satisfy num_seqs >= 0, Hq, Hkv, max_blocks_per_seq, num_blocks >= 1");
-  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq (%d) is not a multiple of Hkv (%d)", Hq, Hkv);
-  if (!finite_positive(scale)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (block_size != 16) return fail(ATTN_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
-  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", d);
-  if (Hq / Hkv > 16) return fail(ATTN_ERR_UNSUPPORTED, "Hq/Hkv = %d > 16 not supported", Hq / Hkv);
-  if (static_cast<long long>(num_blocks) * Hkv * block_size >= 0x7fffffffLL)
-    return fail(ATTN_ERR_UNSUPPORTED, "KV pool too large (num_blocks * Hkv * 16 >= 2^31)");
-  if (static_cast<long long>(max_blocks_per_seq) * block_size >= 0x7fffffffLL)
-    return fail(ATTN_ERR_UNSUPPORTED, "max_blocks_per_seq too large");
+  attn_status_t st = decode_check_args(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv,
+                                       d, block_size, max_blocks_per_seq, num_blocks, scale, o, lse);
+  if (st != ATTN_OK) return st;
   if (num_seqs == 0) {
     g_last_error[0] = '\0';
     return ATTN_OK;
   }
-  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !workspace)
-    return fail(ATTN_ERR_INVALID_ARG, "q, caches, block_table, seq_lens, o, workspace must be non-null");
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace))
-    return fail(ATTN_ERR_INVALID_ARG, "q, caches, o and workspace must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return fail(ATTN_ERR_INVALID_ARG, "block_table, seq_lens and lse must be 4-byte aligned");
+  if (!workspace) return fail(ATTN_ERR_INVALID_ARG, "workspace must be non-null");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   const size_t need = attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq);
   if (workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+  const DecodeBytes nb = decode_bytes(num_seqs, Hq, Hkv, d, max_blocks_per_seq, num_blocks);
+  const struct {
+    const void* p;
+    size_t n;
+  } others[] = {{q, nb.q}, {k_cache, nb.cache}, {v_cache, nb.cache}, {block_table, nb.table},
+                {seq_lens, nb.lens}, {o, nb.o}, {lse, lse ? nb.lse : 0}};
+  for (const auto& x : others)
+    if (x.n && overlap(workspace, need, x.p, x.n))
+      return fail(ATTN_ERR_INVALID_ARG, "workspace overlaps an input or output of the decode");
   DeviceInfo* dev = nullptr;
-  attn_status_t st = current_device(&dev);
-  if (st != ATTN_OK) return st;
-
-  const cuuint32_t box[2] = {64, 16};
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
-                              static_cast<cuuint64_t>(num_blocks) * Hkv * block_size};
-  alignas(64) CUtensorMap tk, tv;
-  if ((st = encode_bf16(&tk, k_cache, 2, dims, box)) != ATTN_OK) return st;
-  if ((st = encode_bf16(&tv, v_cache, 2, dims, box)) != ATTN_OK) return st;
-
-  attn47::DecLaunch a;
-  a.tk = &tk;
-  a.tv = &tv;
-  a.q = q;
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.block_table = block_table;
-  a.seq_lens = seq_lens;
-  a.o = o;
-  a.lse = lse;
-  a.workspace = static_cast<float*>(workspace);
-  a.num_seqs = num_seqs;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.d = d;
-  a.max_blocks = max_blocks_per_seq;
-  a.num_blocks = num_blocks;
-  a.sms = dev->sms;
-  a.max_ctas = g_decode_max_ctas;
-  a.scale = scale;
-  a.status = dev->status;
-  a.timeout_ns = g_timeout_ns;
-  a.stream = static_cast<cudaStream_t>(stream);
-  return launch_result(attn47::launch_decode_sm103(a), "attn_decode_paged");
+  if ((st = current_device(&dev)) != ATTN_OK) return st;
+  if ((st = check_bufs(*dev, {{workspace, need, "workspace"}})) != ATTN_OK) return st;
+  return decode_launch(*dev, q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
+                       max_blocks_per_seq, num_blocks, scale, o, lse, workspace, stream);
 }
 
 attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, const void* v_cache,
@@ -377,19 +498,24 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
                                         int num_seqs, int Hq, int Hkv, int d, int block_size,
                                         int max_blocks_per_seq, int num_blocks, float scale,
                                         void* o, float* lse, void* stream) {
+  // The same argument checks as attn_decode_paged first, so that both calls
+  // give the same answer to the same bad arguments; only then the size of
+  // the scratch this decode needs against the built-in array.
+  attn_status_t st = decode_check_args(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv,
+                                       d, block_size, max_blocks_per_seq, num_blocks, scale, o, lse);
+  if (st != ATTN_OK) return st;
+  if (num_seqs == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
   const size_t need = attn_decode_paged_workspace_size(num_seqs, Hq, d, max_blocks_per_seq);
   if (need > kNoAllocScratchBytes)
     return fail(ATTN_ERR_WORKSPACE,
                 "this decode needs %zu bytes of scratch but the built-in array of "
                 "attn_decode_paged_noalloc holds %zu; call attn_decode_paged with a workspace",
                 need, kNoAllocScratchBytes);
-  if (num_seqs <= 0 || need == 0)   // empty or invalid sizes: same answer as attn_decode_paged
-    return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
-                             block_size, max_blocks_per_seq, num_blocks, scale, o, lse, nullptr,
-                             0, stream);
   DeviceInfo* dev = nullptr;
-  attn_status_t st = current_device(&dev);
-  if (st != ATTN_OK) return st;
+  if ((st = current_device(&dev)) != ATTN_OK) return st;
   void* scratch = nullptr;
   {
     // One-time set-up per device (this device is current): the host-side
@@ -404,9 +530,8 @@ attn_status_t attn_decode_paged_noalloc(const void* q, const void* k_cache, cons
     }
     scratch = dev->noalloc_scratch;
   }
-  return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
-                           block_size, max_blocks_per_seq, num_blocks, scale, o, lse, scratch,
-                           kNoAllocScratchBytes, stream);
+  return decode_launch(*dev, q, k_cache, v_cache, block_table, seq_lens, num_seqs, Hq, Hkv, d,
+                       max_blocks_per_seq, num_blocks, scale, o, lse, scratch, stream);
 }
 
 attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v_new,
@@ -444,6 +569,18 @@ attn_status_t attn_prefill_paged(const void* q, const void* k_new, const void* v
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  {
+    const size_t qb = static_cast<size_t>(num_seqs) * Hq * N * d * 2;
+    const size_t kvb = static_cast<size_t>(num_seqs) * Hkv * N * d * 2;
+    const size_t cb = static_cast<size_t>(num_blocks) * Hkv * 16 * d * 2;
+    if ((st = check_bufs(*dev, {{q, qb, "q"}, {k_new, kvb, "k_new"}, {v_new, kvb, "v_new"},
+                                {k_cache, cb, "k_cache"}, {v_cache, cb, "v_cache"},
+                                {block_table, static_cast<size_t>(num_seqs) * max_blocks_per_seq * 4,
+                                 "block_table"},
+                                {ctx_lens, static_cast<size_t>(num_seqs) * 4, "ctx_lens"}, {o, qb, "o"},
+                                {lse, static_cast<size_t>(num_seqs) * Hq * N * 4, "lse"}})) != ATTN_OK)
+      return st;
+  }
 
   // Q goes through TMA; the kernel gathers the cached K/V blocks itself.
   const cuuint32_t qbox[3] = {64, static_cast<cuuint32_t>(attn47::fwd_box_rows()), 1};
@@ -521,6 +658,9 @@ attn_status_t fused_add_rmsnorm(const void* x, void* residual, const void* weigh
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  if ((st = check_bufs(*dev, {{x, bytes, "x"}, {residual, bytes, "residual"},
+                              {weight, static_cast<size_t>(hidden) * 2, "weight"}, {out, bytes, "out"}})) != ATTN_OK)
+    return st;
   attn47::NormLaunch a;
   a.x = x;
   a.residual = residual;
@@ -549,6 +689,9 @@ attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  if ((st = check_bufs(*dev, {{gate_up, static_cast<size_t>(rows) * F * 4, "gate_up"},
+                              {out, static_cast<size_t>(rows) * F * 2, "out"}})) != ATTN_OK)
+    return st;
   attn47::GluLaunch a;
   a.gate_up = gate_up;
   a.out = out;
@@ -596,6 +739,16 @@ attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, co
   DeviceInfo* dev = nullptr;
   attn_status_t st = current_device(&dev);
   if (st != ATTN_OK) return st;
+  {
+    const size_t xb = static_cast<size_t>(batch) * L * H * P * 2;
+    const size_t bcb = static_cast<size_t>(batch) * L * G * N * 2;
+    const size_t hb = static_cast<size_t>(batch) * H * P * N * 4;
+    if ((st = check_bufs(*dev, {{x, xb, "x"}, {dt, static_cast<size_t>(batch) * L * H * 4, "dt"},
+                                {A, static_cast<size_t>(H) * 4, "A"}, {B, bcb, "B"}, {C, bcb, "C"},
+                                {h0, hb, "h0"}, {y, xb, "y"}, {h_final, hb, "h_final"},
+                                {workspace, need, "workspace"}})) != ATTN_OK)
+      return st;
+  }
   attn47::SsdLaunch a;
   a.x = x;
   a.dt = dt;

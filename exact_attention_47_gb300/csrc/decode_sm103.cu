@@ -743,7 +743,8 @@ int decode_max_parts(int max_blocks_per_seq) {
   // The start cost of a run lies before its block 0, and every later chunk
   // covers at least kMinChunk of its blocks, so the n blocks of one
   // (sequence, KV head) meet at most ceil(n / kMinChunk) + 1 chunks.
-  return (max_blocks_per_seq + kMinChunk - 1) / kMinChunk + 1;
+  // (in 64 bits: max_blocks_per_seq may be anything up to INT_MAX here)
+  return static_cast<int>((static_cast<long long>(max_blocks_per_seq) + kMinChunk - 1) / kMinChunk + 1);
 }
 
 size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq) {

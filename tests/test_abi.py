@@ -147,3 +147,45 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_binding, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _binding.load_library(str(tmp_path / "missing.so"))
+
+
+def test_decode_workspace_must_not_overlap_other_buffers(lib):
+    S, Hq, d, mb = 2, 12, 128, 4
+    need = lib.attn_decode_paged_workspace_size(S, Hq, d, mb)
+    ws = ctypes.c_void_p(0x100000)
+    q, o = ctypes.c_void_p(0x200000), ctypes.c_void_p(0x300000)
+    lse = ctypes.c_void_p(0x400000)
+
+    def call(q_=q, o_=o, lse_=lse, ws_=ws):
+        return lib.attn_decode_paged(q_, FAKE, FAKE, ctypes.c_void_p(0x500000), ctypes.c_void_p(0x600000),
+                                     S, Hq, 2, d, 16, mb, 8, 0.1, o_, lse_, ws_, need, None)
+
+    assert call(o_=ctypes.c_void_p(0x100000 + 1024)) == INVALID      # o inside the workspace
+    assert "overlaps" in lib.attn_last_error().decode()
+    assert call(lse_=ctypes.c_void_p(0x100000 + need - 16)) == INVALID
+    assert call(q_=ctypes.c_void_p(0x100000 - 1024)) == INVALID      # q runs into the workspace
+    assert call(ws_=FAKE) == INVALID                                 # the caches start at FAKE
+
+
+def _noalloc(lib, S=2, Hq=12, Hkv=2, d=128, bs=16, mb=4, nb=8):
+    return lib.attn_decode_paged_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, S, Hq, Hkv, d, bs, mb, nb, 0.1,
+                                         FAKE, None, None)
+
+
+def test_noalloc_checks_arguments_like_the_workspace_entry_point(lib):
+    # The argument checks come before the scratch size: the same bad
+    # arguments give the same status from both decode entry points.
+    for kw, want in ((dict(bs=8), UNSUPPORTED), (dict(d=80), UNSUPPORTED), (dict(Hq=34, Hkv=2), UNSUPPORTED),
+                     (dict(Hq=12, Hkv=5), INVALID), (dict(mb=0), INVALID), (dict(S=-1), INVALID),
+                     (dict(mb=2 ** 31 - 1), UNSUPPORTED), (dict(S=0), OK)):
+        assert _noalloc(lib, **kw) == want, kw
+        assert _dec(lib, **kw) == want, kw
+    # Valid arguments whose scratch exceeds the built-in 8 MiB array.
+    assert _noalloc(lib, S=64, Hq=12, mb=4096) == WORKSPACE
+    assert "8388608" in lib.attn_last_error().decode()
+
+
+def test_decode_workspace_size_has_no_overflow(lib):
+    # ceil(max_blocks / 16) + 1 parts per (sequence, head), computed in 64 bits
+    parts = (2 ** 31 - 1 + 15) // 16 + 1
+    assert lib.attn_decode_paged_workspace_size(1, 1, 128, 2 ** 31 - 1) == parts * 130 * 4 + 4

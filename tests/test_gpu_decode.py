@@ -6,6 +6,8 @@ the ragged lengths around block edges, empty sequences, NaN in unused slots,
 paging invariances, and the device-side checks of bad table entries.
 """
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -154,8 +156,18 @@ def test_bad_seq_len_is_clamped_and_reported():
 def test_small_workspace_is_rejected():
     inp = workloads.decode_inputs(2, 12, 2, 128, seed=29, len_lo=1, len_hi=64)
     ws = torch.empty(64, dtype=torch.uint8, device=DEV)
-    with pytest.raises(attn.AttnError, match="WORKSPACE"):
+    with pytest.raises(ValueError, match="workspace has 64 bytes"):      # the binding's check
         run(inp, 0.1, workspace=ws)
+    d = to_dev(inp)
+    o = torch.empty_like(d["q"])
+    S, Hq, dh = d["q"].shape
+    nb, Hkv = d["k_cache"].shape[:2]
+    p = [ctypes.c_void_p(d[n].data_ptr()) for n in ("q", "k_cache", "v_cache", "block_table", "seq_lens")]
+    st = attn.load_library().attn_decode_paged(*p, S, Hq, Hkv, dh, 16, d["block_table"].shape[1], nb, 0.1,
+                                               ctypes.c_void_p(o.data_ptr()), None,
+                                               ctypes.c_void_p(ws.data_ptr()), 64,
+                                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 5                                                       # the C-ABI's: ATTN_ERR_WORKSPACE
 
 
 def test_bounded_wait_times_out_and_reports():
