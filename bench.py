@@ -13,6 +13,8 @@ Also timed, outside the step and reported under their own keys:
                      Qwen-style GQA, block_size 16, permuted table)
   fusions            fused_add_rmsnorm and fused_swiglu on a Qwen2.5-1.5B-sized
                      layer over 16384 tokens (HBM GB/s)
+  ssd                ssd_chunked_fwd (Mamba-2 SSD forward) on a Mamba-2-2.7B-
+                     sized layer: batch 4, L 4096, 80 heads of 64, state 128
 Printed (rank 0, one JSON line): fwd TFLOP/s as `value` (causal flops
 4*B*Hq*N^2*d/2 over the forward kernel's CUDA-event time), the decode's HBM
 GB/s (algorithmic bytes over its kernels' time) under "decode", rooflines
@@ -51,13 +53,41 @@ FWD_CFG = "qwen_gqa_prefill"
 DEC_CFG = "paged_decode"
 NSETS = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed
-# ncu summaries (profiles/), taken on this workload; None once a kernel changes
-# until it is captured again.  Medians over the 10 bench-step launches of one
-# capture (launches_all_bench_workloads.md).  Forward: reads are q + k + v;
-# writes vary with what o and lse leave in L2.  Decode: main kernel + merge.
-TRAFFIC_FWD = 67192448 + 4752640
-TRAFFIC_DEC = (132293888 + 192384) + (3272192 + 0)
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the bench step's
+# kernels, from one single-kernel ncu capture of this workload (profiles/),
+# valid only for the kernel source it was taken on: each entry keeps the
+# sha256 of its source files at capture time, and bench reports the traffic
+# as null once those files differ.
+CSRC = os.path.join(ROOT, "exact_attention_47_gb300", "csrc")
+TRAFFIC = {
+    # median read + median write of 3 launches
+    "fwd": {"bytes": 67195136 + 5155072, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
+            "sha256": "c34e733b18ef16ed00df4bf8aab02bb3a237eb07e9774a402cd207357f993b6f"},
+    # decode kernel + merge kernel, medians of 3 launches each
+    "dec": {"bytes": (132293888 + 228096) + (3272192 + 0),
+            "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
+            "sha256": "1ee64ce39e977a55269b55a183e6ea9a65b79ec848a19c579892b982a2a7cbaf"},
+}
+
+
+def source_digest(files):
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_for(key):
+    """(bytes per launch or None, why) for a bench-step kernel."""
+    rec = TRAFFIC[key]
+    if rec["bytes"] is None or rec["sha256"] is None:
+        return None, "not captured for this kernel source"
+    if source_digest(rec["sources"]) != rec["sha256"]:
+        return None, "kernel source changed since the capture"
+    return rec["bytes"], "ncu capture of this kernel source (sha256 %s...)" % rec["sha256"][:12]
 
 
 def peaks():
@@ -398,6 +428,66 @@ def fusion_bytes(rows, hidden, F):
     return {"add_rmsnorm": 4 * rows * hidden * 2 + hidden * 2, "swiglu": 3 * rows * F * 2}
 
 
+def ssd_flops(batch, L, H, P, N, chunk):
+    """FLOPs of the chunked SSD forward per call, by the matrix form: per
+    (batch, head) and chunk of n positions, C B^T under the causal mask and
+    its product with X (n^2/2 pairs each: n^2 N + n^2 P), the state update
+    (x o w)^T B and the carried state's output C S^T (2 n P N each)."""
+    total = 0
+    for c0 in range(0, L, chunk):
+        n = min(chunk, L - c0)
+        total += n * n * (N + P) + 4 * n * P * N
+    return float(batch * H * total)
+
+
+def ssd_bytes(batch, L, H, G, P, N):
+    """Algorithmic bytes per call: x, B, C (bf16), dt (fp32) and A read; y
+    (bf16) and the final state (fp32) written."""
+    return (batch * L * H * P * 2 + 2 * batch * L * G * N * 2 + batch * L * H * 4 + H * 4
+            + batch * L * H * P * 2 + batch * H * P * N * 4)
+
+
+def ssd_measurement(attn, device, steps, peak_tflops, peak_gbs):
+    """ssd_chunked_fwd on the mamba2_ssd workload (x and y are 168 MB each,
+    beyond L2), CUDA events over `steps` calls after 3 warm-ups.  Reported
+    against both rooflines; its intensity sits near the ridge."""
+    c = workloads.SSD_CONFIGS["mamba2_ssd"]
+    d = workloads.ssd_inputs(c["batch"], c["L"], c["H"], c["P"], c["N"], c["G"], c["seed"])
+    d = {k: v.to(device) for k, v in d.items()}
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((c["batch"], c["H"], c["P"], c["N"]), dtype=torch.float32, device=device)
+    ws = torch.empty(attn.ssd_workspace_size(c["batch"], c["L"], c["H"], c["N"], c["chunk"]),
+                     dtype=torch.uint8, device=device)
+
+    def call():
+        attn.ssd_chunked_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], chunk=c["chunk"], y=y,
+                             h_final=hf, workspace=ws)
+
+    for _ in range(3):
+        call()
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = ssd_flops(c["batch"], c["L"], c["H"], c["P"], c["N"], c["chunk"])
+    nbytes = ssd_bytes(c["batch"], c["L"], c["H"], c["G"], c["P"], c["N"])
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = nbytes / (ms / 1e3) / 1e9
+    bound = "tensor" if flops / peak_tflops / 1e12 >= nbytes / peak_gbs / 1e9 else "hbm"
+    del d, y, hf, ws
+    return {"workload": "mamba2_ssd (batch 4, L 4096, H 80, P 64, N 128, G 1, chunk 256)", "ms": ms,
+            "tflops": tflops, "frac_tensor": tflops / peak_tflops, "GB/s": gbs, "frac_hbm": gbs / peak_gbs,
+            "bound": bound, "flops": flops, "bytes": nbytes,
+            "flop_convention": "per chunk of n: n^2 (N + P) + 4 n P N (causal pairs n^2/2)",
+            "kernels": "chunk cumsum + fwd_pass_state + chunk output", "gpu_launches_per_call": 3}
+
+
 def fusion_measurement(attn, device, steps, peak_gbs):
     """fused_add_rmsnorm and fused_swiglu on one Qwen2.5-1.5B-sized layer over
     the 16384 prefill tokens (hidden 1536, intermediate 8960), CUDA events over
@@ -544,10 +634,12 @@ def run_gpu(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1) / K
     clock.stop()
     pk_all, _ = peaks()
-    fwd_configs = fwd_config_table(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
-    backward = bwd_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
-    paged_prefill = paged_prefill_measurement(attn, device, max(10, K // 2), pk_all["bf16_tflops"])
-    fusions = fusion_measurement(attn, device, max(10, K // 2), pk_all["hbm_gbs"])
+    side = max(10, min(K, 200))      # calls per measurement outside the step
+    fwd_configs = fwd_config_table(attn, device, side, pk_all["bf16_tflops"])
+    backward = bwd_measurement(attn, device, side, pk_all["bf16_tflops"])
+    paged_prefill = paged_prefill_measurement(attn, device, side, pk_all["bf16_tflops"])
+    fusions = fusion_measurement(attn, device, side, pk_all["hbm_gbs"])
+    ssd = ssd_measurement(attn, device, side, pk_all["bf16_tflops"], pk_all["hbm_gbs"])
 
     # ---- max over ranks
     total_ms, fwd_sum, dec_sum, e2e_ms = max_over_ranks(
@@ -556,9 +648,16 @@ def run_gpu(args, rank, world, local_rank):
     if rank == 0:
         pk, pk_kind = peaks()
         tflops, gbs, achieved_fwd, achieved_dec = job_rates(world, K, flops, dbytes, fwd_sum, dec_sum)
+        clocks = clock.summary(wall0, wall1)
+        traffic_fwd, traffic_fwd_src = traffic_for("fwd")
+        traffic_dec, traffic_dec_src = traffic_for("dec")
+        # time x median SM clock (ms x MHz = thousands of SM cycles): comparable
+        # across runs whose clocks differ
+        kcyc = (lambda ms: None if clocks.get("sm_mhz") is None else ms * clocks["sm_mhz"])
         line = {
             "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+            "kcycles_per_step": kcyc(total_ms / K),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": "%s (B4 Hq12 Hkv2 N4096 d128 causal) + %s (64 seqs, Hq12 "
@@ -568,7 +667,9 @@ def run_gpu(args, rank, world, local_rank):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved_fwd,
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": achieved_fwd / pk["bf16_tflops"], "traffic": TRAFFIC_FWD,
+                         "frac": achieved_fwd / pk["bf16_tflops"], "traffic": traffic_fwd,
+                         "traffic_source": traffic_fwd_src,
+                         "kcycles_per_launch": kcyc(fwd_sum / K),
                          "kernel": "attn_fwd_sm103_kernel<128,causal>",
                          "peak_kind": pk_kind + " burst bf16 (cuBLAS)",
                          "fwd_ms_mean": fwd_sum / K, "fwd_ms_median": statistics.median(fwd_ms)},
@@ -576,7 +677,8 @@ def run_gpu(args, rank, world, local_rank):
                        "ms_median": statistics.median(dec_ms), "bytes_per_step": dbytes,
                        "roofline": {"bound": "hbm", "achieved": achieved_dec,
                                     "peak": pk["hbm_gbs"], "unit": "GB/s",
-                                    "frac": achieved_dec / pk["hbm_gbs"], "traffic": TRAFFIC_DEC,
+                                    "frac": achieved_dec / pk["hbm_gbs"], "traffic": traffic_dec,
+                                    "traffic_source": traffic_dec_src,
                                     "kernel": "attn_decode_paged_kernel<128> + combine",
                                     "peak_kind": pk_kind + " copy bandwidth"}},
             "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
@@ -589,8 +691,10 @@ def run_gpu(args, rank, world, local_rank):
             "backward": backward,
             "paged_prefill": paged_prefill,
             "fusions": fusions,
+            "ssd": ssd,
             "gpu_launches": 3 * K,
-            "clocks": clock.summary(wall0, wall1),
+            "timed_region_s": total_ms / 1e3,
+            "clocks": clocks,
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_sample(args.cpu_seconds)
@@ -603,8 +707,8 @@ def run_gpu(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=6000)     # about 1.4 s of GPU time
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

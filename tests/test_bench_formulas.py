@@ -51,3 +51,26 @@ def test_fusion_byte_counts():
     got = bench.fusion_bytes(rows, hidden, F)
     assert got["add_rmsnorm"] == x + residual_in + residual_out + out + weight
     assert got["swiglu"] == gate_up + act
+
+
+def test_ssd_flops_counts_the_matrix_form():
+    # Per (batch, head) and chunk of n positions: the masked C B^T and its
+    # product with X over n^2/2 pairs (N and P multiply-adds each), the
+    # state update and the carried state's output (P N multiply-adds per
+    # position each).
+    batch, L, H, P, N, chunk = 2, 300, 3, 8, 16, 128
+    total = 0
+    for c0 in range(0, L, chunk):
+        n = min(chunk, L - c0)
+        pairs = n * n / 2
+        total += pairs * 2 * N + pairs * 2 * P      # C B^T, then (.) X
+        total += n * 2 * P * N + n * 2 * P * N      # (x w)^T B, C S^T
+    assert bench.ssd_flops(batch, L, H, P, N, chunk) == batch * H * total
+
+
+def test_ssd_bytes_lists_every_tensor():
+    batch, L, H, G, P, N = 2, 300, 4, 2, 64, 128
+    d = workloads.ssd_inputs(batch, L, H, P, N, G, seed=1)
+    reads = sum(t.numel() * t.element_size() for t in d.values())      # x, dt, A, B, C
+    writes = batch * L * H * P * 2 + batch * H * P * N * 4             # y (bf16), final state (fp32)
+    assert bench.ssd_bytes(batch, L, H, G, P, N) == reads + writes
