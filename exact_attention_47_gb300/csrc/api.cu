@@ -42,6 +42,7 @@ attn_status_t fail(attn_status_t s, const char* fmt, ...) {
 }
 
 unsigned long long g_timeout_ns = 1000000000ull;
+
 int g_decode_max_ctas = 0;  // 0 = one full wave
 
 constexpr int kMaxDevices = 64;
@@ -185,6 +186,19 @@ attn_status_t encode_bf16(CUtensorMap* map, const void* base, int rank, const cu
   return ATTN_OK;
 }
 
+// bf16 tensor map with explicit byte strides of dims 1.. (innermost dim
+// contiguous), 128-byte swizzle, zero fill out of bounds.
+attn_status_t encode_bf16_strided(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                                  const cuuint64_t* strides, const cuuint32_t* box) {
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ATTN_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return ATTN_OK;
+}
+
 attn_status_t launch_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(ATTN_ERR_LAUNCH, "%s launch failed: %s", what, cudaGetErrorString(e));
   g_last_error[0] = '\0';
@@ -248,11 +262,14 @@ attn_status_t decode_launch(const DeviceInfo& dev, const void* q, const void* k_
                                       {v_cache, nb.cache, "v_cache"}, {block_table, nb.table, "block_table"},
                                       {seq_lens, nb.lens, "seq_lens"}, {o, nb.o, "o"}, {lse, nb.lse, "lse"}});
   if (st != ATTN_OK) return st;
-  const cuuint32_t box[2] = {64, 16};
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(num_blocks) * Hkv * 16};
+  // One copy per (block, head) slice: 64 columns x 16 rows x d/64 halves.
+  const cuuint32_t box[3] = {64, 16, static_cast<cuuint32_t>(d / 64)};
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * Hkv * 16,
+                              static_cast<cuuint64_t>(d / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
   alignas(64) CUtensorMap tk, tv;
-  if ((st = encode_bf16(&tk, k_cache, 2, dims, box)) != ATTN_OK) return st;
-  if ((st = encode_bf16(&tv, v_cache, 2, dims, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16_strided(&tk, k_cache, 3, dims, strides, box)) != ATTN_OK) return st;
+  if ((st = encode_bf16_strided(&tv, v_cache, 3, dims, strides, box)) != ATTN_OK) return st;
 
   attn47::DecLaunch a;
   a.tk = &tk;

@@ -14,15 +14,17 @@
 // whatever the length mix.  The chunk is walked as segments (maximal runs of
 // one (b, g)); the G = Hq/Hkv query heads sharing KV head g are processed
 // together so each K/V block is read from HBM once.
-//   warp 4      producer: plans the chunk from seq_lens; translates table
+//   warp 7      producer: plans the chunk from seq_lens; translates table
 //               entries a batch of 32 blocks ahead; per segment bulk-copies
-//               the G query rows; per
-//               block TMA-copies the (block, head) K and V slices (16 x d
-//               bf16, 128-byte swizzle) into an 8-stage ring
-//   warps 0..3  consumers: block c of the chunk goes to warp c % 4; scores
-//               and P V are 16x8x16 warp MMAs (rows = the G query heads,
-//               zero-padded to 16); at the segment's end the four warp states
-//               are merged in shared memory
+//               the G query rows; per block TMA-copies the (block, head) K
+//               and V slices (16 x d bf16, 128-byte swizzle; one copy each)
+//               into a ring of 21 stages (14 when G > 8)
+//   warps 0..6  consumers: block c of the chunk goes to warp c % 7, which
+//               moves its K and V fragments to registers and hands the stage
+//               back before computing; scores and P V are 16x8x16 warp MMAs
+//               (rows = the G query heads, zero-padded to 16); at the
+//               segment's end the seven warp states are merged in shared
+//               memory
 // A segment that covers a whole sequence writes O and LSE directly; the
 // others write an unnormalised partial (O, max, sum), and a second kernel
 // (launched as a programmatic dependent) merges the parts of each sequence.
@@ -35,47 +37,73 @@ namespace attn47 {
 namespace {
 
 constexpr int kBS = 16;          // block_size (token slots per physical block)
-constexpr int kConsumers = 4;    // consumer warps
+// Eight warps: seven consumers and one producer, two warps per SM
+// sub-partition (so each may hold up to 255 registers).
+constexpr int kConsumers = 7;
 constexpr int kThreads = (kConsumers + 1) * 32;
-// Block c of a CTA's chunk goes to stage c % 8 and consumer warp c % 4, so
-// each stage is only ever read by one warp, in the order it is filled (the
-// parity of a stage's barrier can then never be mistaken for a later fill).
-constexpr int kStages = 8;
-constexpr int kQSlots = 2;
+// Block c of a CTA's chunk goes to stage c % kStages and consumer warp
+// c % 7 (kStages a multiple of 7), so each stage is only ever read by one
+// warp, in the order it is filled (the parity of a stage's barrier can then
+// never be mistaken for a later fill).
+template <int GM>
+constexpr int stages_for() { return GM <= 8 ? 21 : 14; }
+constexpr int kMaxStages = 21;
+// Block counts of the first kSeqCache sequences, kept in shared memory by the
+// plan so that the walks over the chunk read no global memory.
+constexpr int kSeqCache = 1024;
+// Lazy stabiliser: a row's running maximum (log2 units) only moves when a
+// block's maximum exceeds it by more than this, so most blocks skip the
+// rescale of O; numerators then lie in [0, 2^kTau].
+constexpr float kTau = 8.f;
+constexpr int kQSlots = 8;
 constexpr int kMinChunk = 2 * kMinSplitBlocks;   // block-heads per CTA, lower bound
-// A CTA pays about this many blocks' worth of time to start a (sequence,
-// KV head) run (query load, state merge, output write), so work is split by
-// cost = blocks + kRunCost per run, not by blocks alone.
-constexpr int kRunCost = 3;
+// A CTA pays about this many blocks' worth of time for a (sequence, KV
+// head) run (query rows, the merge of the warp states, the output write, and
+// the warps' uneven finish at the run's end), so work is split by cost =
+// blocks + kRunCost per run, not by blocks alone.  Measured: 3, 6, 10 and 15
+// gave 37.5, 37.0, 37.3 and 36.8 us on 64 sequences of U[128, 4096] tokens
+// and 51.0, 48.6, 47.3 and 46.2 us on 256 of U[32, 1024].
+constexpr int kRunCost = 15;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+// Shared-memory layout for head dim D and groups of at most GM query heads
+// per KV head (8 or 16).
+template <int D, int GM>
 struct DecLayout {
-  static constexpr int kChunks = D / 64;
+  static constexpr int kStages = stages_for<GM>();
   static constexpr int kBox = kBS * 128;          // one 64-column box of a block: 2 KB
   static constexpr int kHalf = kBS * D * 2;       // K (or V) slice of one (block, head)
   static constexpr int kStage = 2 * kHalf;
   static constexpr int kRing = kStages * kStage;
-  static constexpr int kQSlot = 16 * D * 2;       // up to 16 query heads of one (b, g)
+  static constexpr int kQSlot = GM * D * 2;       // the query heads of one (b, g)
   static constexpr int kOffQ = kRing;
   static constexpr int kOffComb = kOffQ + kQSlots * kQSlot;
-  static constexpr int kComb = kConsumers * 16 * (D + 2) * 4;
-  static constexpr int kOffShared = kOffComb + kComb;
-  static constexpr int kSmem = kOffShared + 256 + 1024;     // + alignment slack
+  // Merge buffer of a segment's end: every warp's O rows, then every warp's
+  // (max, sum) per row.
+  static constexpr int kComb = kConsumers * GM * (D + 2) * 4;
+  static constexpr int kOffCache = kOffComb + kComb;
+  static constexpr int kOffShared = kOffCache + kSeqCache * 4;
+  static constexpr int kSmem = kOffShared + 1024 + 1024;    // + alignment slack
+  static_assert(kStages % kConsumers == 0, "a stage must map to one consumer warp");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 struct DecShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t qfull[kQSlots];
   uint64_t qempty[kQSlots];
-  int phys[kStages];
+  int phys[kMaxStages];
+  int fills[kMaxStages];        // fills issued per stage (for the final drain)
+  int qfills[kQSlots];          // fills issued per query slot
+  uint64_t comb_free;           // merge buffer free again (its segment merged)
+  int comb_cnt;                 // warps that wrote their state into the buffer
   int c0, c1, chunk, b0, off0;
   int cost0;                    // first cost unit of this CTA (chunk is in cost units)
+  int pseq0;                    // cost position of the first sequence's first run
   int abort;
 };
-static_assert(sizeof(DecShared) <= 256, "shared control block");
-static_assert(kStages % kConsumers == 0, "a stage must map to one consumer warp");
+static_assert(sizeof(DecShared) <= 1024, "shared control block");
 
 struct DecParams {
   const __nv_bfloat16* q;
@@ -87,7 +115,7 @@ struct DecParams {
   float* lse;
   float* ws_o;
   float* ws_ml;
-  int* nparts;
+  int* nparts;                    // parts per (sequence, KV head), for the merge kernel
   int num_seqs, Hq, Hkv, group, max_blocks, num_blocks, max_parts;
   float scale_log2;
   unsigned int* status;
@@ -101,18 +129,26 @@ __device__ __forceinline__ int seq_len(const DecParams& p, int b) {
 __device__ __forceinline__ int seq_blocks(const DecParams& p, int b) {
   return (seq_len(p, b) + kBS - 1) / kBS;
 }
+__device__ __forceinline__ int seq_blocks(const DecParams& p, const int* cache, int b) {
+  return b < kSeqCache ? cache[b] : seq_blocks(p, b);
+}
 
 // Deterministic walk over the segments of one CTA's chunk; the producer and
 // the consumers each run their own copy.
 struct SegWalk {
   int b, g, blk, nblk, remaining, flat;
-  __device__ void start(const DecParams& p, int b0, int off0, int c0, int c1) {
+  int pcost;   // cost position where the current run starts (its start cost first)
+  const int* cache;
+  __device__ void start(const DecParams& p, const int* nb_cache, int b0, int off0, int c0, int c1,
+                        int pseq) {
+    cache = nb_cache;
     b = b0;
-    nblk = seq_blocks(p, b0);
+    nblk = seq_blocks(p, cache, b0);
     g = off0 / nblk;
     blk = off0 % nblk;
     remaining = c1 - c0;
     flat = c0;
+    pcost = pseq + g * (nblk + kRunCost);
   }
   // Current segment: blocks [blk, blk + count()) of (b, g).
   __device__ int count() const { return min(remaining, nblk - blk); }
@@ -135,29 +171,115 @@ struct SegWalk {
     remaining -= cnt;
     flat += cnt;
     blk = 0;
+    pcost += nblk + kRunCost;      // runs follow each other in cost order
     if (++g == p.Hkv) {
       g = 0;
       do {
         ++b;
-        nblk = (remaining > 0 && b < p.num_seqs) ? seq_blocks(p, b) : 1;
+        nblk = (remaining > 0 && b < p.num_seqs) ? seq_blocks(p, cache, b) : 1;
       } while (remaining > 0 && nblk == 0);
     }
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads)
+// Merge of one segment by one warp: the seven consumer warps' states of the
+// segment (rows < G of the merge buffer) combined into O and the LSE when the
+// segment is a whole run, else into this CTA's partial of the run, and the
+// run's part count recorded by the holder of part 0 for the merge kernel.
+// Lane l owns columns [l D/32, (l + 1) D/32).
+template <int D, int GM>
+__device__ __forceinline__ void merge_segment(const DecParams& p, const float* cbo, const float* cbm,
+                                              const SegWalk& w, int chunk, int G, int lane) {
+  constexpr int E = D / 32;
+  // The run's parts are the CTAs holding its blocks, cost positions
+  // pcost + kRunCost .. pcost + kRunCost + nblk - 1 (CTA x holds
+  // [x chunk, (x + 1) chunk)); this CTA's part index counts from the first.
+  const int first_cta = (w.pcost + kRunCost) / chunk;
+  const int nparts = (w.pcost + kRunCost + w.nblk - 1) / chunk - first_cta + 1;
+  const int part = static_cast<int>(blockIdx.x) - first_cta;
+  const bool whole = nparts == 1;
+  const bool in_range = part >= 0 && part < nparts && nparts <= p.max_parts;
+  const size_t hq0 = static_cast<size_t>(w.b) * p.Hq + w.g * G;
+#pragma unroll
+  for (int r = 0; r < GM; ++r) {
+    if (r >= G) break;
+    // Every lane reads the seven (max, sum) pairs of the row (shared-memory
+    // broadcasts) and forms the weights itself: no cross-lane chains, and
+    // the rows are independent of each other.
+    float mw[kConsumers], M = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kConsumers; ++ww) {
+      mw[ww] = cbm[(ww * GM + r) * 2];
+      M = fmaxf(M, mw[ww]);
+    }
+    float acc[E], lsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < kConsumers; ++ww) {
+        const float wt = ex2(mw[ww] - M);
+        lsum += wt * cbm[(ww * GM + r) * 2 + 1];
+        const float* src = cbo + (ww * GM + r) * D + lane * E;
+        if constexpr (E == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          acc[0] += wt * v.x;
+          acc[1] += wt * v.y;
+          acc[2] += wt * v.z;
+          acc[3] += wt * v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          acc[0] += wt * v.x;
+          acc[1] += wt * v.y;
+        }
+      }
+    }
+    const size_t hq = hq0 + r;
+    if (whole) {
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      if constexpr (E == 4) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(p.o + hq * D + lane * E) = pk;
+      } else {
+        *reinterpret_cast<uint32_t*>(p.o + hq * D + lane * E) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      }
+      if (lane == 0 && p.lse != nullptr) p.lse[hq] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
+    } else if (in_range) {
+      const size_t slot = hq * p.max_parts + part;
+      if constexpr (E == 4)
+        *reinterpret_cast<float4*>(p.ws_o + slot * D + lane * E) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      else
+        *reinterpret_cast<float2*>(p.ws_o + slot * D + lane * E) = make_float2(acc[0], acc[1]);
+      if (lane == 0) {
+        p.ws_ml[slot * 2 + 0] = M;
+        p.ws_ml[slot * 2 + 1] = lsum;
+      }
+    }
+  }
+  // The holder of part 0 records the run's part count for the merge kernel
+  // (1: the run was written here, nothing to merge).
+  if (part == 0 && lane == 0) {
+    p.nparts[static_cast<size_t>(w.b) * p.Hkv + w.g] = (whole || !in_range) ? 1 : nparts;
+    if (!in_range) atomicOr(p.status, kDevTimeout);   // cannot happen: the split bounds nparts
+  }
+}
+
+template <int D, int GM>
+__global__ void __launch_bounds__(kThreads, 1)
     attn_decode_paged_kernel(const __grid_constant__ CUtensorMap tk,
                              const __grid_constant__ CUtensorMap tv, const DecParams p) {
-  using Lt = DecLayout<D>;
+  using Lt = DecLayout<D, GM>;
+  constexpr int kStages = Lt::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   DecShared* sh = reinterpret_cast<DecShared*>(smem + Lt::kOffShared);
   const uint32_t ring = smem_addr(smem);
   const uint32_t qring = smem_addr(smem + Lt::kOffQ);
-  float* comb = reinterpret_cast<float*>(smem + Lt::kOffComb);   // [4][16][D]
-  float* cml = comb + kConsumers * 16 * D;                          // [4][16][2]
+  float* comb = reinterpret_cast<float*>(smem + Lt::kOffComb);   // [warps][GM][D], then [warps][GM][2]
+  int* nb_cache = reinterpret_cast<int*>(smem + Lt::kOffCache);   // [kSeqCache] blocks per sequence
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -169,6 +291,24 @@ __global__ void __launch_bounds__(kThreads)
   // CTA takes the cost units [cost0, cost0 + chunk), chunk = max(kMinChunk,
   // ceil(C / grid)), and with them the blocks [c0, c1) in flat order: the
   // start cost of a run sits just before its block 0.
+  if (warp == kConsumers && lane == 0) {
+    prefetch_tmap(&tk);
+    prefetch_tmap(&tv);
+    // Bring this CTA's share of the block table and of the queries into L2
+    // while the plan reads the sequence lengths (16-byte aligned interior).
+    auto prefetch_share = [&](const void* base, size_t bytes) {
+      const uintptr_t lo = (reinterpret_cast<uintptr_t>(base) + 15) & ~static_cast<uintptr_t>(15);
+      const uintptr_t hi = (reinterpret_cast<uintptr_t>(base) + bytes) & ~static_cast<uintptr_t>(15);
+      if (hi <= lo) return;
+      const size_t share = (((hi - lo) / gridDim.x) + 16) & ~static_cast<size_t>(15);
+      const uintptr_t a = lo + share * blockIdx.x;
+      if (a >= hi) return;
+      const size_t n = min(share, static_cast<size_t>(hi - a));
+      bulk_prefetch_l2(reinterpret_cast<const void*>(a), static_cast<uint32_t>(n));
+    };
+    prefetch_share(p.block_table, static_cast<size_t>(p.num_seqs) * p.max_blocks * 4);
+    prefetch_share(p.q, static_cast<size_t>(p.num_seqs) * p.Hq * D * 2);
+  }
   if (warp == kConsumers) {
     int T = 0, C = 0;
     bool bad = false;
@@ -181,6 +321,7 @@ __global__ void __launch_bounds__(kThreads)
         bad |= (L < 0 || L > p.max_blocks * kBS);
         const int Lc = L < 0 ? 0 : min(L, p.max_blocks * kBS);
         const int blocks = (Lc + kBS - 1) / kBS;
+        if (b < kSeqCache && b < p.num_seqs) nb_cache[b] = blocks;
         nb[u] = blocks * p.Hkv;
         nc[u] = blocks > 0 ? (blocks + kRunCost) * p.Hkv : 0;
       }
@@ -196,20 +337,22 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0)
       atomicOr(p.status, kDevBadSeqLen);
+    __syncwarp();                                // the cache entries of every lane
     const int grid = static_cast<int>(gridDim.x);
     const int chunk = max(kMinChunk, (C + grid - 1) / grid);
     const int cost0 = static_cast<int>(blockIdx.x) * chunk;
     const int cost1 = min(C, cost0 + chunk);
     // Flat block position (and sequence, offset in it) of a cost position.
-    auto locate = [&](int cost, int& flat, int& bq, int& off) {
+    auto locate = [&](int cost, int& flat, int& bq, int& off, int& pseq) {
       flat = T;
       bq = -1;
       off = 0;
+      pseq = 0;
       if (cost >= C) return;
       int P = 0, F = 0;
       for (int base = 0; base < p.num_seqs && bq < 0; base += 32) {
         const int b = base + lane;
-        const int blocks = (b < p.num_seqs) ? seq_blocks(p, b) : 0;
+        const int blocks = (b < p.num_seqs) ? seq_blocks(p, nb_cache, b) : 0;
         const int nc = blocks > 0 ? (blocks + kRunCost) * p.Hkv : 0;
         int incl = nc, fincl = blocks * p.Hkv;
 #pragma unroll
@@ -228,7 +371,8 @@ __global__ void __launch_bounds__(kThreads)
           const int src = __ffs(hit) - 1;
           bq = base + src;
           const int nblk = __shfl_sync(0xffffffffu, blocks, src);
-          const int rel = cost - P - __shfl_sync(0xffffffffu, excl, src);
+          pseq = P + __shfl_sync(0xffffffffu, excl, src);
+          const int rel = cost - pseq;
           const int g = rel / (nblk + kRunCost);
           const int blk = max(0, rel % (nblk + kRunCost) - kRunCost);
           off = g * nblk + blk;
@@ -238,9 +382,9 @@ __global__ void __launch_bounds__(kThreads)
         F += __shfl_sync(0xffffffffu, fincl, 31);
       }
     };
-    int c0, b0, off0, c1, b1, off1;
-    locate(cost0, c0, b0, off0);
-    locate(cost1, c1, b1, off1);
+    int c0, b0, off0, c1, b1, off1, pseq0, pseq1;
+    locate(cost0, c0, b0, off0, pseq0);
+    locate(cost1, c1, b1, off1, pseq1);
     if (lane == 0) {
       sh->c0 = c0;
       sh->c1 = c1;
@@ -248,6 +392,7 @@ __global__ void __launch_bounds__(kThreads)
       sh->b0 = (c0 < c1) ? b0 : -1;
       sh->off0 = off0;
       sh->cost0 = cost0;
+      sh->pseq0 = pseq0;
     }
   }
   if (threadIdx.x == 0) {
@@ -258,26 +403,34 @@ __global__ void __launch_bounds__(kThreads)
     for (int s = 0; s < kQSlots; ++s) {
       mbar_init(smem_addr(&sh->qfull[s]), 1);
       mbar_init(smem_addr(&sh->qempty[s]), 1);
+      sh->qfills[s] = 0;
     }
+    for (int s = 0; s < kMaxStages; ++s) sh->fills[s] = 0;
+    mbar_init(smem_addr(&sh->comb_free), 1);
+    sh->comb_cnt = 0;
+
     sh->abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  // Let the merge kernel launch; it waits for this grid before reading.
-  pdl_launch_dependents();
   const int c0 = sh->c0, c1 = sh->c1, chunk = sh->chunk, b0 = sh->b0, off0 = sh->off0;
-  const int cost0 = sh->cost0;
+  const int pseq0 = sh->pseq0;
   if (c0 >= c1 || b0 < 0) return;                 // whole CTA: no work
   const WaitCtl wc{&sh->abort, p.status, p.timeout_ns};
 
   if (warp == kConsumers) {
     // ------------------------------------------------------------ producer
-    // Lane j handles chunk blocks j, 32 + j, 64 + j, ...: it translates the
-    // table entry up to a batch of 32 blocks before the block is copied, so
-    // no table lookup sits between two copies.
+    // The chunk is issued in batches of 32 blocks, lane j owning block j of
+    // the batch: its table entry is translated two batches ahead into its
+    // registers, and the batch goes out in four rounds of 8 lanes, each lane
+    // waiting for its own stage and issuing its own copies, so the per-block
+    // cost of the loop is shared by 8 blocks.  A lane whose block starts a
+    // segment first copies that segment's query rows into slot (segment % 8);
+    // with 8 slots, the wait for a slot only ever depends on blocks issued in
+    // earlier rounds.
     const int nblocks = c1 - c0;
     SegWalk lw;
-    lw.start(p, b0, off0, c0, c1);
+    lw.start(p, nb_cache, b0, off0, c0, c1, pseq0);
     lw.skip(p, lane);
     auto fetch = [&](int k, int& ph, int& bb, int& gg) {
       ph = -1;
@@ -286,84 +439,99 @@ __global__ void __launch_bounds__(kThreads)
       if (k < nblocks && lw.remaining > 0) {
         bb = lw.b;
         gg = lw.g;
+        // The entry is checked where it is used, so this load stays in
+        // flight while the walk moves on.
         ph = p.block_table[static_cast<size_t>(lw.b) * p.max_blocks + lw.blk];
-        if (ph < 0 || ph >= p.num_blocks) {
-          atomicOr(p.status, kDevBadBlock);
-          ph = -1;
-        }
       }
+      lw.skip(p, 32);
     };
-    // The first batch is translated before the loop; each next one a few
-    // copies into the current batch, so the first copy leaves at once.
-    int cur_ph, cur_b, cur_g, nxt_ph = -1, nxt_b = -1, nxt_g = 0;
+    int cur_ph, cur_b, cur_g, n1_ph, n1_b, n1_g, n2_ph, n2_b, n2_g;
     fetch(lane, cur_ph, cur_b, cur_g);
+    fetch(32 + lane, n1_ph, n1_b, n1_g);
+    fetch(64 + lane, n2_ph, n2_b, n2_g);
 
-    int issued = 0, seg = 0, pb = -1, pg = -1;
+    int seg = 0, carry_b = -1, carry_g = -1;
     bool ok = true;
     const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
-    for (int c = 0; c < nblocks && ok; ++c) {
-      const int j = c & 31;
-      if (j == 0 && c > 0) {
-        cur_ph = nxt_ph;
-        cur_b = nxt_b;
-        cur_g = nxt_g;
-      }
-      if (j == 4) {
-        lw.skip(p, 32);
-        fetch(c - 4 + 32 + lane, nxt_ph, nxt_b, nxt_g);
-      }
-      const int phys = __shfl_sync(0xffffffffu, cur_ph, j);
-      const int b = __shfl_sync(0xffffffffu, cur_b, j);
-      const int g = __shfl_sync(0xffffffffu, cur_g, j);
+    for (int base = 0; base < nblocks && ok; base += 32) {
+      const int cblk = base + lane;
+      const bool valid = cblk < nblocks;
+      // Segment starts: (b, g) differs from the previous block's.
+      int prev_b = __shfl_up_sync(0xffffffffu, cur_b, 1);
+      int prev_g = __shfl_up_sync(0xffffffffu, cur_g, 1);
       if (lane == 0) {
-        if (b != pb || g != pg) {
-          // First block of a segment: its query rows.
-          const int qs = seg % kQSlots;
-          ok = mbar_wait(smem_addr(&sh->qempty[qs]), ((seg / kQSlots) & 1) ^ 1, wc);
-          if (ok) {
-            const uint32_t qb = smem_addr(&sh->qfull[qs]);
-            mbar_arrive_expect_tx(qb, qbytes);
-            bulk_load(qring + qs * Lt::kQSlot, p.q + (static_cast<size_t>(b) * p.Hq + g * G) * D,
-                      qbytes, qb);
-          }
-          ++seg;
-          pb = b;
-          pg = g;
-        }
-        const int st = issued % kStages;
-        if (ok) ok = mbar_wait(smem_addr(&sh->empty[st]), ((issued / kStages) & 1) ^ 1, wc);
-        if (ok) {
-          const uint32_t fb = smem_addr(&sh->full[st]);
-          sh->phys[st] = phys;
-          if (phys >= 0) {
-            const int rowk = (phys * p.Hkv + g) * kBS;
-            const uint32_t dst = ring + st * Lt::kStage;
-            mbar_arrive_expect_tx(fb, Lt::kStage);
-#pragma unroll
-            for (int cc = 0; cc < Lt::kChunks; ++cc) {
-              tma_load_2d(dst + cc * Lt::kBox, &tk, fb, cc * 64, rowk);
-              tma_load_2d(dst + Lt::kHalf + cc * Lt::kBox, &tv, fb, cc * 64, rowk);
+        prev_b = carry_b;
+        prev_g = carry_g;
+      }
+      const bool start = valid && (cur_b != prev_b || cur_g != prev_g);
+      const unsigned smask = __ballot_sync(0xffffffffu, start);
+      const int sego = seg + __popc(smask & ((1u << lane) - 1u));
+      seg += __popc(smask);
+      carry_b = __shfl_sync(0xffffffffu, cur_b, 31);
+      carry_g = __shfl_sync(0xffffffffu, cur_g, 31);
+      const int st = cblk % kStages;
+      const int fill = cblk / kStages;
+#pragma unroll 1
+      for (int r = 0; r < 4; ++r) {
+        bool okl = true;
+        if (valid && (lane >> 3) == r) {
+          if (start) {
+            const int qs = sego % kQSlots;
+            okl = mbar_wait(smem_addr(&sh->qempty[qs]), ((sego / kQSlots) & 1) ^ 1, wc);
+            if (okl) {
+              const uint32_t qb = smem_addr(&sh->qfull[qs]);
+              mbar_arrive_expect_tx(qb, qbytes);
+              bulk_load(qring + qs * Lt::kQSlot,
+                        p.q + (static_cast<size_t>(cur_b) * p.Hq + cur_g * G) * D, qbytes, qb);
+              sh->qfills[qs] = sego / kQSlots + 1;
             }
-          } else {
-            mbar_arrive(fb);
           }
-          ++issued;
+          if (okl) okl = mbar_wait(smem_addr(&sh->empty[st]), (fill & 1) ^ 1, wc);
+          if (okl) {
+            if (cur_ph < 0 || cur_ph >= p.num_blocks) {
+              atomicOr(p.status, kDevBadBlock);    // outside the pool: that block is skipped
+              cur_ph = -1;
+            }
+            const uint32_t fb = smem_addr(&sh->full[st]);
+            sh->phys[st] = cur_ph;
+            sh->fills[st] = fill + 1;
+            if (cur_ph >= 0) {
+              const int rowk = (cur_ph * p.Hkv + cur_g) * kBS;
+              const uint32_t dst = ring + st * Lt::kStage;
+              mbar_arrive_expect_tx(fb, Lt::kStage);
+              tma_load_3d(dst, &tk, fb, 0, rowk, 0);
+              tma_load_3d(dst + Lt::kHalf, &tv, fb, 0, rowk, 0);
+            } else {
+              mbar_arrive(fb);
+            }
+          }
+        }
+        if (!__all_sync(0xffffffffu, okl)) {
+          ok = false;
+          break;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      cur_ph = n1_ph;
+      cur_b = n1_b;
+      cur_g = n1_g;
+      n1_ph = n2_ph;
+      n1_b = n2_b;
+      n1_g = n2_g;
+      fetch(base + 96 + lane, n2_ph, n2_b, n2_g);
     }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
-    seg = __shfl_sync(0xffffffffu, seg, 0);
-    // Every copy issued must have landed before the CTA may exit.
-    if (lane == 0) {
-      for (int st = 0; st < kStages && st < issued; ++st) {
-        const int fills = (issued - 1 - st) / kStages + 1;
-        mbar_wait(smem_addr(&sh->full[st]), (fills - 1) & 1, wc, true);
-      }
-      for (int qs = 0; qs < kQSlots && qs < seg; ++qs) {
-        const int fills = (seg - 1 - qs) / kQSlots + 1;
-        mbar_wait(smem_addr(&sh->qfull[qs]), (fills - 1) & 1, wc, true);
-      }
+    __syncwarp();
+    // Every copy is issued: the merge kernel may launch (it waits for this
+    // grid to finish before reading).
+    pdl_launch_dependents();
+    // Every copy issued must have landed before the CTA may exit: wait for
+    // the last fill of every stage and query slot.
+    if (lane < kStages) {
+      const int fills = sh->fills[lane];
+      if (fills > 0) mbar_wait(smem_addr(&sh->full[lane]), (fills - 1) & 1, wc, true);
+    }
+    if (lane < kQSlots) {
+      const int fills = sh->qfills[lane];
+      if (fills > 0) mbar_wait(smem_addr(&sh->qfull[lane]), (fills - 1) & 1, wc, true);
     }
   } else {
     // ----------------------------------------------------------- consumers
@@ -371,7 +539,7 @@ __global__ void __launch_bounds__(kThreads)
     const int r0 = lane >> 2;               // fragment row (query head within the group)
     const int cq = (lane & 3) * 2;          // fragment column pair
     SegWalk w;
-    w.start(p, b0, off0, c0, c1);
+    w.start(p, nb_cache, b0, off0, c0, c1, pseq0);
     int base_blk = 0, seg = 0;
     while (w.remaining > 0) {
       const int cnt = w.count();
@@ -404,52 +572,76 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
-      for (int i = (warp - base_blk) & (kConsumers - 1); i < cnt && !fail; i += kConsumers) {
+      for (int i = ((warp - base_blk) % kConsumers + kConsumers) % kConsumers; i < cnt && !fail;
+           i += kConsumers) {
         const int gi = base_blk + i;            // block counter of the whole chunk
         const int st = gi % kStages;
         if (!mbar_wait_warp(smem_addr(&sh->full[st]), (gi / kStages) & 1, wc)) { fail = true; break; }
         const int ph = sh->phys[st];
         const int nvalid = min(kBS, L - (w.blk + i) * kBS);
+        // K and V fragments of this block go to registers first, so the
+        // stage is handed back to the producer before any arithmetic.
+        uint32_t kf[2][D / 32][4];      // B operand of S = Q K^T: [key tile][d step]
+        uint32_t vf[D / 16][4];         // B operand of O += P V (transposed load)
         if (ph >= 0) {
           const uint32_t sK = ring + st * Lt::kStage;
           const uint32_t sV = sK + Lt::kHalf;
-          if (nvalid < kBS) {
-            // Slots past the sequence end may hold anything (even NaN): zero
-            // their V rows so that P = 0 cannot meet NaN in the MMA.
-            const int words = (kBS - nvalid) * Lt::kChunks * 8;
-            for (int idx = lane; idx < words; idx += 32) {
-              const int rr = nvalid + idx / (Lt::kChunks * 8);
-              const int rem = idx % (Lt::kChunks * 8);
-              const uint32_t a = sV + (rem >> 3) * Lt::kBox + rr * 128 + (rem & 7) * 16;
-              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
-            }
-            __syncwarp();
-          }
-          // S = Q K^T : two 8-key column tiles.
-          float sc[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
             const int key = nt * 8 + (lane & 7);
 #pragma unroll
             for (int kk2 = 0; kk2 < D / 32; ++kk2) {
               const int c = 4 * kk2 + (lane >> 3);
-              const uint32_t addr =
-                  sK + (c >> 3) * Lt::kBox + key * 128 + (((c & 7) ^ (key & 7)) << 4);
-              uint32_t bb[4];
-              ldsm_x4(addr, bb);
-              mma_16816(sc[nt], qa[2 * kk2], bb[0], bb[1]);
-              mma_16816(sc[nt], qa[2 * kk2 + 1], bb[2], bb[3]);
+              ldsm_x4(sK + (c >> 3) * Lt::kBox + key * 128 + (((c & 7) ^ (key & 7)) << 4), kf[nt][kk2]);
             }
           }
-          // Mask slots past the end, running max / sum, rescale O.
+          const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+          for (int dt2 = 0; dt2 < D / 16; ++dt2) {
+            const int c = 2 * dt2 + (lane >> 4);
+            ldsm_x4_trans(sV + (c >> 3) * Lt::kBox + vkey * 128 + (((c & 7) ^ (vkey & 7)) << 4), vf[dt2]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sh->empty[st]));
+        if (ph >= 0) {
+          if (nvalid < kBS) {
+            // Slots past the sequence end may hold anything (even NaN): zero
+            // their V values so that P = 0 cannot meet NaN in the MMA.  This
+            // lane's halves hold keys 2(lane%4) + {0,1} (registers 0, 2) and
+            // 8 + 2(lane%4) + {0,1} (registers 1, 3).
+            const int k0 = 2 * (lane & 3);
+            const uint32_t m_lo = (k0 < nvalid ? 0x0000ffffu : 0u) | (k0 + 1 < nvalid ? 0xffff0000u : 0u);
+            const uint32_t m_hi = (k0 + 8 < nvalid ? 0x0000ffffu : 0u) | (k0 + 9 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int dt2 = 0; dt2 < D / 16; ++dt2) {
+              vf[dt2][0] &= m_lo;
+              vf[dt2][2] &= m_lo;
+              vf[dt2][1] &= m_hi;
+              vf[dt2][3] &= m_hi;
+            }
+          }
+          // S = Q K^T: two 8-key column tiles, each over two independent
+          // accumulator chains (even and odd 16-wide d steps).
+          float sc[2][4], sd[2][4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
+#pragma unroll
+            for (int kk2 = 0; kk2 < D / 32; ++kk2) {
+              mma_16816(sc[nt], qa[2 * kk2], kf[nt][kk2][0], kf[nt][kk2][1]);
+              mma_16816(sd[nt], qa[2 * kk2 + 1], kf[nt][kk2][2], kf[nt][kk2][3]);
+            }
+          }
+          // Mask slots past the end; lazy running max, sums.
           float x[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int kl = nt * 8 + cq + (e & 1);
-              x[nt][e] = (kl < nvalid) ? sc[nt][e] * sl2 : -INFINITY;
+              x[nt][e] = (kl < nvalid) ? (sc[nt][e] + sd[nt][e]) * sl2 : -INFINITY;
             }
           float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
           float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -457,109 +649,89 @@ __global__ void __launch_bounds__(kThreads)
           mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
           mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-          const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);   // finite: slot 0 is valid
-          const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);
+          // The stabiliser moves only when the block's maximum exceeds it by
+          // more than kTau (always on the first block: m = -inf); slot 0 of
+          // every block is valid, so the maxima are finite.
+          const bool up0 = mx0 > m0 + kTau, up1 = mx1 > m1 + kTau;
+          if (__any_sync(0xffffffffu, up0 || up1)) {
+            const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+            const float a0 = ex2(m0 - mn0), a1 = ex2(m1 - mn1);
+            l0 *= a0;
+            l1 *= a1;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) {
+              oacc[dt][0] *= a0;
+              oacc[dt][1] *= a0;
+              oacc[dt][2] *= a1;
+              oacc[dt][3] *= a1;
+            }
+          }
           float pr[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            pr[nt][0] = ex2(x[nt][0] - mn0);
-            pr[nt][1] = ex2(x[nt][1] - mn0);
-            pr[nt][2] = ex2(x[nt][2] - mn1);
-            pr[nt][3] = ex2(x[nt][3] - mn1);
+            pr[nt][0] = ex2(x[nt][0] - m0);
+            pr[nt][1] = ex2(x[nt][1] - m0);
+            pr[nt][2] = ex2(x[nt][2] - m1);
+            pr[nt][3] = ex2(x[nt][3] - m1);
           }
-          l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-          l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-          m0 = mn0;
-          m1 = mn1;
-#pragma unroll
-          for (int dt = 0; dt < D / 8; ++dt) {
-            oacc[dt][0] *= a0;
-            oacc[dt][1] *= a0;
-            oacc[dt][2] *= a1;
-            oacc[dt][3] *= a1;
-          }
+          l0 += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+          l1 += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
           // The score accumulator layout is the A-operand layout of P.
           uint32_t pa[4];
           pa[0] = pack_bf16x2(pr[0][0], pr[0][1]);
           pa[1] = pack_bf16x2(pr[0][2], pr[0][3]);
           pa[2] = pack_bf16x2(pr[1][0], pr[1][1]);
           pa[3] = pack_bf16x2(pr[1][2], pr[1][3]);
-          // O += P V : V rows are keys, transposed on load.
-          const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
           for (int dt2 = 0; dt2 < D / 16; ++dt2) {
-            const int c = 2 * dt2 + (lane >> 4);
-            const uint32_t addr =
-                sV + (c >> 3) * Lt::kBox + vkey * 128 + (((c & 7) ^ (vkey & 7)) << 4);
-            uint32_t bb[4];
-            ldsm_x4_trans(addr, bb);
-            mma_16816(oacc[2 * dt2], pa, bb[0], bb[1]);
-            mma_16816(oacc[2 * dt2 + 1], pa, bb[2], bb[3]);
+            mma_16816(oacc[2 * dt2], pa, vf[dt2][0], vf[dt2][1]);
+            mma_16816(oacc[2 * dt2 + 1], pa, vf[dt2][2], vf[dt2][3]);
           }
-          if (nvalid < kBS) fence_proxy_async_smem();   // zeroed rows before the next TMA write
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sh->empty[st]));
       }
       l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
       l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
       l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-      // ---------------------------------- merge the four warp states
+      if (fail) break;
+      // ------------------------ hand the warp state to the segment's merge
+      // Every warp writes its state into the merge buffer and goes on with
+      // the next segment; the last of the seven to arrive merges them, so
+      // no warp waits for the others at a segment's end.  The buffer is
+      // reused by the next segment once that merge is done.
+      if (!mbar_wait_warp(smem_addr(&sh->comb_free), (seg & 1) ^ 1, wc)) break;
+      float* cml = comb + kConsumers * GM * D;          // [warps][GM][2]
 #pragma unroll
       for (int dt = 0; dt < D / 8; ++dt) {
         const int d = dt * 8 + cq;
-        *reinterpret_cast<float2*>(&comb[(warp * 16 + r0) * D + d]) =
-            make_float2(oacc[dt][0], oacc[dt][1]);
-        *reinterpret_cast<float2*>(&comb[(warp * 16 + r0 + 8) * D + d]) =
-            make_float2(oacc[dt][2], oacc[dt][3]);
+        *reinterpret_cast<float2*>(&comb[(warp * GM + r0) * D + d]) = make_float2(oacc[dt][0], oacc[dt][1]);
+        if (r0 + 8 < GM)
+          *reinterpret_cast<float2*>(&comb[(warp * GM + r0 + 8) * D + d]) = make_float2(oacc[dt][2], oacc[dt][3]);
       }
       if ((lane & 3) == 0) {
-        cml[(warp * 16 + r0) * 2 + 0] = m0;
-        cml[(warp * 16 + r0) * 2 + 1] = l0;
-        cml[(warp * 16 + r0 + 8) * 2 + 0] = m1;
-        cml[(warp * 16 + r0 + 8) * 2 + 1] = l1;
-      }
-      // All consumers stop together if any of them failed or the CTA aborted.
-      if (named_barrier_or(1, kConsumers * 32, fail || *wc.abort)) break;
-      if (threadIdx.x == 0) mbar_arrive(smem_addr(&sh->qempty[qs]));
-      const bool last = (w.blk + cnt == w.nblk);
-      const bool whole = (w.blk == 0) && last;
-      // Part index = this CTA - the CTA holding block 0 of the run.  Only the
-      // first segment can continue a run: its block 0 sits at cost position
-      // cost0 - w.blk, in CTA (cost0 - w.blk) / chunk.
-      const int part = (w.blk > 0) ? static_cast<int>(blockIdx.x) - (cost0 - w.blk) / chunk : 0;
-      for (int idx = threadIdx.x; idx < G * D; idx += kConsumers * 32) {
-        const int r = idx / D;
-        const int d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int ww = 0; ww < kConsumers; ++ww) M = fmaxf(M, cml[(ww * 16 + r) * 2]);
-        float acc = 0.f, lsum = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int ww = 0; ww < kConsumers; ++ww) {
-            const float wt = ex2(cml[(ww * 16 + r) * 2] - M);
-            acc += wt * comb[(ww * 16 + r) * D + d];
-            lsum += wt * cml[(ww * 16 + r) * 2 + 1];
-          }
-        }
-        const size_t hq = static_cast<size_t>(w.b) * p.Hq + w.g * G + r;
-        if (whole) {
-          p.o[hq * D + d] = __float2bfloat16_rn(lsum > 0.f ? acc / lsum : 0.f);
-          if (d == 0 && p.lse != nullptr)
-            p.lse[hq] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
-        } else {
-          const size_t slot = hq * p.max_parts + part;
-          p.ws_o[slot * D + d] = acc;
-          if (d == 0) {
-            p.ws_ml[slot * 2 + 0] = M;
-            p.ws_ml[slot * 2 + 1] = lsum;
-          }
+        cml[(warp * GM + r0) * 2 + 0] = m0;
+        cml[(warp * GM + r0) * 2 + 1] = l0;
+        if (r0 + 8 < GM) {
+          cml[(warp * GM + r0 + 8) * 2 + 0] = m1;
+          cml[(warp * GM + r0 + 8) * 2 + 1] = l1;
         }
       }
-      if (last && threadIdx.x == 0) p.nparts[w.b * p.Hkv + w.g] = part + 1;
-      named_barrier_sync(1, kConsumers * 32);      // merge buffer free again
+      __threadfence_block();
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) arrived = atomicAdd(&sh->comb_cnt, 1);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived == kConsumers - 1) {
+        __threadfence_block();
+        merge_segment<D, GM>(p, comb, cml, w, chunk, G, lane);
+        if (lane == 0) {
+          sh->comb_cnt = 0;
+          mbar_arrive(smem_addr(&sh->qempty[qs]));
+          mbar_arrive(smem_addr(&sh->comb_free));
+        }
+      }
       base_blk += cnt;
       w.advance(p, cnt);
       ++seg;
@@ -671,10 +843,10 @@ __global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineP
     p.lse[static_cast<size_t>(b) * p.Hq + h] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
 }
 
-template <int D>
+template <int D, int GM>
 cudaError_t launch_t(const DecLaunch& a) {
-  using Lt = DecLayout<D>;
-  auto kern = attn_decode_paged_kernel<D>;
+  using Lt = DecLayout<D, GM>;
+  auto kern = attn_decode_paged_kernel<D, GM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lt::kSmem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -733,6 +905,11 @@ cudaError_t launch_t(const DecLaunch& a) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // Same shared-memory carveout as the decode kernel, so that the SMs need
+  // no reconfiguration between the two (or before the next decode).
+  e = cudaFuncSetAttribute(attn_decode_combine_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   e = cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<D>, c);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -748,13 +925,18 @@ int decode_max_parts(int max_blocks_per_seq) {
 }
 
 size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq) {
+  // Partial O (d floats), max and sum per (sequence, query head, part), then
+  // the part count of every (sequence, KV head) (8 bytes per sequence and
+  // query head are reserved for it).
   const size_t parts = static_cast<size_t>(num_seqs) * Hq * decode_max_parts(max_blocks_per_seq);
   return parts * (static_cast<size_t>(d) + 2) * sizeof(float) +
-         static_cast<size_t>(num_seqs) * Hq * sizeof(int);
+         static_cast<size_t>(num_seqs) * Hq * sizeof(unsigned long long);
 }
 
 cudaError_t launch_decode_sm103(const DecLaunch& a) {
-  return a.d == 128 ? launch_t<128>(a) : launch_t<64>(a);
+  const bool small_group = a.Hq / a.Hkv <= 8;
+  if (a.d == 128) return small_group ? launch_t<128, 8>(a) : launch_t<128, 16>(a);
+  return small_group ? launch_t<64, 8>(a) : launch_t<64, 16>(a);
 }
 
 }  // namespace attn47

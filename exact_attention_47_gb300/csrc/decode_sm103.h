@@ -12,7 +12,11 @@ namespace attn47 {
 constexpr int kMinSplitBlocks = 8;
 
 struct DecLaunch {
-  const CUtensorMap* tk;   // [num_blocks*Hkv*16, d] bf16, box {64, 16}, 128-byte swizzle
+  // Cache maps, 3-D {64 columns, num_blocks*Hkv*16 rows (stride d*2 bytes),
+  // d/64 column halves (stride 128 bytes)}, box {64, 16, d/64}, 128-byte
+  // swizzle: one copy lands a whole (block, head) slice as d/64 swizzled
+  // 16 x 64 tiles.
+  const CUtensorMap* tk;
   const CUtensorMap* tv;
   const void* q;           // [num_seqs, Hq, d] bf16
   const void* k_cache;     // [num_blocks, Hkv, 16, d] bf16

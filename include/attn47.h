@@ -160,9 +160,10 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
 /*
  * attn_decode_paged_workspace_size — bytes of device workspace that
- * attn_decode_paged needs for these sizes (fp32 partial results of
- * sequences whose keys are split across CTAs, and a count per sequence).
- * 0 for an empty problem.
+ * attn_decode_paged needs for these sizes: fp32 partial results of
+ * sequences whose keys are split across CTAs, and their part counts (8 bytes
+ * per sequence and query head are reserved for these).  0 for an empty
+ * problem.
  */
 size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blocks_per_seq);
 
@@ -187,9 +188,11 @@ size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blo
  *  block_size must be 16; d must be 64 or 128; Hq % Hkv == 0 and
  *  Hq / Hkv <= 16; num_blocks * Hkv * 16 < 2^31.
  *  num_seqs == 0 is an empty problem: returns ATTN_OK, launches nothing.
- *  Launches two kernels (decode over an even split of all cached tokens,
- *  then the merge of sequences split across CTAs).  Deterministic for a
- *  given device and attn_set_decode_max_ctas setting.
+ *  Launches two kernels: the decode over an even split of all cached tokens
+ *  (one CTA per SM), then the merge, in a fixed order, of the parts of
+ *  sequences split across CTAs.  Calls that share a workspace must not
+ *  overlap on the GPU.  Deterministic for a given device and
+ *  attn_set_decode_max_ctas setting.
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                                 const int32_t* block_table, const int32_t* seq_lens, int num_seqs,

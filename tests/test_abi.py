@@ -138,8 +138,9 @@ def test_ssd_host_validation(lib):
 
 def test_workspace_size_formula(lib):
     # fp32 partial O (d floats) + max and sum per (seq, head, part) with at
-    # most ceil(256 / 16) + 1 parts, plus one int count per (seq, head)
-    assert lib.attn_decode_paged_workspace_size(64, 12, 128, 256) == 64 * 12 * 17 * 130 * 4 + 64 * 12 * 4
+    # most ceil(256 / 16) + 1 parts, plus 8 bytes per (seq, head) reserved
+    # for the part counts
+    assert lib.attn_decode_paged_workspace_size(64, 12, 128, 256) == 64 * 12 * 17 * 130 * 4 + 64 * 12 * 8
     assert lib.attn_decode_paged_workspace_size(0, 12, 128, 256) == 0
 
 
@@ -188,4 +189,4 @@ def test_noalloc_checks_arguments_like_the_workspace_entry_point(lib):
 def test_decode_workspace_size_has_no_overflow(lib):
     # ceil(max_blocks / 16) + 1 parts per (sequence, head), computed in 64 bits
     parts = (2 ** 31 - 1 + 15) // 16 + 1
-    assert lib.attn_decode_paged_workspace_size(1, 1, 128, 2 ** 31 - 1) == parts * 130 * 4 + 4
+    assert lib.attn_decode_paged_workspace_size(1, 1, 128, 2 ** 31 - 1) == parts * 130 * 4 + 8
