@@ -604,8 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Row maximum: a depth-5 tree of three-input maxima.
-      float mx;
-      {
+      auto row_max = [&]() {
         float t[43], u[15];
 #pragma unroll
         for (int i = 0; i < 42; ++i) t[i] = fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
@@ -613,13 +612,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 14; ++i) u[i] = fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
         u[14] = t[42];
-        mx = fmaxf(fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmax3(u[6], u[7], u[8])),
-                   fmax3(fmax3(u[9], u[10], u[11]), u[12], fmaxf(u[13], u[14])));
-      }
-      const float mt = mx * sl2;
-      if (j == 0) {
-        m = (mt == -INFINITY) ? 0.f : mt;
-      } else {
+        return fmaxf(fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmax3(u[6], u[7], u[8])),
+                     fmax3(fmax3(u[9], u[10], u[11]), u[12], fmaxf(u[13], u[14])));
+      };
+      // Numerators p = 2^(s * scale * log2 e - m), two lanes per instruction
+      // for the scale and the sums.  Two denominators: `lr` sums the
+      // bf16-rounded numerators that P V uses, so O / lr weights every value
+      // row by exactly the factor it got; `l` sums the fp32 numerators and
+      // gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
+      // 2c+1 in column c), the first half while the second is computed.
+      float lt, lrt;                               // this tile's two sums
+      auto numerators = [&]() {
+        const uint64_t sc2 = f2_pack(sl2, sl2);
+        const uint64_t nm2 = f2_pack(-m, -m);
+        uint64_t accE[4] = {0, 0, 0, 0};
+        float accR[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int e = half * 64 + 2 * c;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), sc2, nm2), x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            const uint32_t w = pack_bf16x2(p0, p1);
+            accE[c & 3] = f2_add(accE[c & 3], f2_pack(p0, p1));
+            accR[(c & 1) * 2] = add_bf16lo_f32(w, accR[(c & 1) * 2]);
+            accR[(c & 1) * 2 + 1] = add_bf16hi_f32(w, accR[(c & 1) * 2 + 1]);
+            pk[c] = w;
+          }
+          ATTN47_TMEM_ST32(tl + colS + half * 32, pk);
+        }
+        float e0, e1;
+        f2_unpack(f2_add(f2_add(accE[0], accE[1]), f2_add(accE[2], accE[3])), e0, e1);
+        lt = e0 + e1;
+        lrt = (accR[0] + accR[1]) + (accR[2] + accR[3]);
+      };
+      // Moves the stabiliser to the tile's maximum where that exceeds it by
+      // more than kTau, rescaling the sums and O_X (which holds PV_X(0..j-1),
+      // complete since S_X(j) completed after it).
+      auto restabilise = [&]() {
+        const float mt = row_max() * sl2;
         const bool need = mt > m + kTau;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m;
@@ -627,7 +661,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           lr *= alpha;
           m = m_new;
-          // O_X holds PV_X(0..j-1), complete since S_X(j) completed after it.
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
@@ -645,40 +678,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ATTN47_TMEM_ST32(tl + colO + c0, o);
           }
         }
-      }
-      // Numerators p = 2^(s * scale * log2 e - m), two lanes per instruction
-      // for the scale and the sums.  Two denominators: `lr` sums the
-      // bf16-rounded numerators that P V uses, so O / lr weights every value
-      // row by exactly the factor it got; `l` sums the fp32 numerators and
-      // gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
-      // 2c+1 in column c), the first half while the second is computed.
-      const uint64_t sc2 = f2_pack(sl2, sl2);
-      const uint64_t nm2 = f2_pack(-m, -m);
-      uint64_t accE[4] = {0, 0, 0, 0};
-      float accR[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int e = half * 64 + 2 * c;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), sc2, nm2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          const uint32_t w = pack_bf16x2(p0, p1);
-          accE[c & 3] = f2_add(accE[c & 3], f2_pack(p0, p1));
-          accR[(c & 1) * 2] = add_bf16lo_f32(w, accR[(c & 1) * 2]);
-          accR[(c & 1) * 2 + 1] = add_bf16hi_f32(w, accR[(c & 1) * 2 + 1]);
-          pk[c] = w;
+      };
+      if (j == 0) {
+        const float mt = row_max() * sl2;
+        m = (mt == -INFINITY) ? 0.f : mt;
+        numerators();
+      } else {
+        // The stabiliser only has to keep the numerators finite (fp32 and
+        // bf16 reach 2^127), so the tile's maximum is not formed up front:
+        // the numerators are computed with the current m, and only a tile
+        // whose fp32 sum exceeds 2^100 (or is not finite) is redone with the
+        // stabiliser moved to its maximum.  Same function, same rounding.
+        numerators();
+        const bool big = !(lt <= 0x1p100f);
+        if (__any_sync(0xffffffffu, big)) {
+          restabilise();
+          numerators();
         }
-        ATTN47_TMEM_ST32(tl + colS + half * 32, pk);
       }
-      {
-        float e0, e1;
-        f2_unpack(f2_add(f2_add(accE[0], accE[1]), f2_add(accE[2], accE[3])), e0, e1);
-        l += e0 + e1;
-        lr += (accR[0] + accR[1]) + (accR[2] + accR[3]);
-      }
+      l += lt;
+      lr += lrt;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
