@@ -454,16 +454,17 @@ def fusion_bytes(rows, hidden, F):
     return {"add_rmsnorm": 4 * rows * hidden * 2 + hidden * 2, "swiglu": 3 * rows * F * 2}
 
 
-def ssd_flops(batch, L, H, P, N, chunk):
+def ssd_flops(batch, L, H, G, P, N, chunk):
     """FLOPs of the chunked SSD forward per call, by the matrix form: per
-    (batch, head) and chunk of n positions, C B^T under the causal mask and
-    its product with X (n^2/2 pairs each: n^2 N + n^2 P), the state update
-    (x o w)^T B and the carried state's output C S^T (2 n P N each)."""
+    chunk of n positions, C B^T under the causal mask once per B/C group
+    (n^2/2 pairs of N multiply-adds: n^2 N), and per head its product with X
+    (n^2 P), the state update (x o w)^T B and the carried state's output
+    C S^T (2 n P N each)."""
     total = 0
     for c0 in range(0, L, chunk):
         n = min(chunk, L - c0)
-        total += n * n * (N + P) + 4 * n * P * N
-    return float(batch * H * total)
+        total += G * n * n * N + H * (n * n * P + 4 * n * P * N)
+    return float(batch * total)
 
 
 def ssd_bytes(batch, L, H, G, P, N):
@@ -501,7 +502,7 @@ def ssd_measurement(attn, device, steps, peak_tflops, peak_gbs):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    flops = ssd_flops(c["batch"], c["L"], c["H"], c["P"], c["N"], c["chunk"])
+    flops = ssd_flops(c["batch"], c["L"], c["H"], c["G"], c["P"], c["N"], c["chunk"])
     nbytes = ssd_bytes(c["batch"], c["L"], c["H"], c["G"], c["P"], c["N"])
     tflops = flops / (ms / 1e3) / 1e12
     gbs = nbytes / (ms / 1e3) / 1e9
@@ -510,8 +511,8 @@ def ssd_measurement(attn, device, steps, peak_tflops, peak_gbs):
     return {"workload": "mamba2_ssd (batch 4, L 4096, H 80, P 64, N 128, G 1, chunk 256)", "ms": ms,
             "tflops": tflops, "frac_tensor": tflops / peak_tflops, "GB/s": gbs, "frac_hbm": gbs / peak_gbs,
             "bound": bound, "flops": flops, "bytes": nbytes,
-            "flop_convention": "per chunk of n: n^2 (N + P) + 4 n P N (causal pairs n^2/2)",
-            "kernels": "chunk cumsum + fwd_pass_state + chunk output", "gpu_launches_per_call": 3}
+            "flop_convention": "per chunk of n: G n^2 N + H (n^2 P + 4 n P N) (causal pairs n^2/2)",
+            "kernels": "chunk state (cumsum + fwd_pass_state) + chunk output", "gpu_launches_per_call": 2}
 
 
 def fusion_measurement(attn, device, steps, peak_gbs):

@@ -748,7 +748,7 @@ attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, co
     return fail(ATTN_ERR_INVALID_ARG, "dt and A must be 4-byte aligned");
   const long long nc = (static_cast<long long>(L) + chunk - 1) / chunk;
   if (static_cast<long long>(batch) * nc * H * (chunk / 64) > 0x7fffffffLL ||
-      static_cast<long long>(batch) * H * (N / 64) > 0x7fffffffLL)
+      static_cast<long long>(batch) * nc * H * P > 0x7fffffffLL || static_cast<long long>(L) + chunk > 0x7fffffffLL)
     return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
   const size_t need = ssd_workspace_size(batch, L, H, N, chunk);
   if (workspace_bytes < need)
@@ -776,12 +776,42 @@ attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, co
   a.y = y;
   a.h_final = h_final;
   a.workspace = workspace;
+  // Tensor maps: x over (P, H, L, batch), B and C over (N, G, L, batch),
+  // the bf16 chunk states in the workspace over (N, batch * nc * H * P).
+  CUtensorMap tx, tb, tc, ts;
+  {
+    const cuuint32_t rows = static_cast<cuuint32_t>(chunk < 128 ? chunk : 128);
+    const cuuint64_t xdims[4] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(H),
+                                 static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(batch)};
+    const cuuint64_t xstr[3] = {static_cast<cuuint64_t>(P) * 2, static_cast<cuuint64_t>(H) * P * 2,
+                                static_cast<cuuint64_t>(L) * H * P * 2};
+    const cuuint32_t xbox[4] = {64, 1, rows, 1};
+    if ((st = encode_bf16_strided(&tx, x, 4, xdims, xstr, xbox)) != ATTN_OK) return st;
+    const cuuint64_t bdims[4] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(G),
+                                 static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(batch)};
+    const cuuint64_t bstr[3] = {static_cast<cuuint64_t>(N) * 2, static_cast<cuuint64_t>(G) * N * 2,
+                                static_cast<cuuint64_t>(L) * G * N * 2};
+    if ((st = encode_bf16_strided(&tb, B, 4, bdims, bstr, xbox)) != ATTN_OK) return st;
+    const cuuint32_t cbox[4] = {64, 1, 128, 1};
+    if ((st = encode_bf16_strided(&tc, C, 4, bdims, bstr, cbox)) != ATTN_OK) return st;
+    const cuuint64_t sdims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(batch * nc * H * P)};
+    const cuuint64_t sstr[1] = {static_cast<cuuint64_t>(N) * 2};
+    const cuuint32_t sbox[2] = {64, 64};
+    const void* states = static_cast<const uint8_t*>(workspace) + attn47::ssd_states_offset(batch, L, H, chunk);
+    if ((st = encode_bf16_strided(&ts, states, 2, sdims, sstr, sbox)) != ATTN_OK) return st;
+  }
+  a.tx = &tx;
+  a.tb = &tb;
+  a.tc = &tc;
+  a.ts = &ts;
   a.batch = batch;
   a.L = L;
   a.H = H;
   a.G = G;
   a.N = N;
   a.chunk = chunk;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_result(attn47::launch_ssd_sm103(a), "ssd_chunked_fwd");
 }

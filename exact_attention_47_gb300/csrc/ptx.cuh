@@ -165,6 +165,12 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, co
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
 
+// Warp-uniform bounded wait that ignores an abort raised by another role:
+// used at exit for work this warp itself started (copies, MMAs).
+__device__ __forceinline__ bool mbar_wait_warp_drain(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, true));
+}
+
 // Per-warpgroup register budget changes (all four warps of a warpgroup).
 template <uint32_t N>
 __device__ __forceinline__ void regs_increase() {
@@ -214,6 +220,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint32_t bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 // Contiguous global -> shared bulk copy (addresses 16-byte aligned, size a
@@ -342,6 +356,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with the major-ness of A chosen too (a_mn_major: A stored with M
+// contiguous, bit 15).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle, tcgen05 version field = 1.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
@@ -383,6 +403,29 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),        \
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),        \
       "r"(r[29]), "r"(r[30]), "r"(r[31])                                                         \
+      : "memory")
+
+// 32 lanes x 16 columns.
+#define ATTN47_TMEM_LD16(taddr, r)                                                               \
+  asm volatile(                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"   \
+      "%14,%15}, [%16];"                                                                         \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),      \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),               \
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                                                    \
+      : "r"(taddr))
+#define ATTN47_TMEM_LD16_WAIT(r)                                                                 \
+  asm volatile("tcgen05.wait::ld.sync.aligned;"                                                  \
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),         \
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),       \
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])::"memory")
+#define ATTN47_TMEM_ST16(taddr, r)                                                               \
+  asm volatile(                                                                                  \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"    \
+      "%13,%14,%15,%16};" ::"r"(taddr),                                                          \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),    \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),          \
+      "r"(r[15])                                                                                 \
       : "memory")
 
 __device__ __forceinline__ void tmem_st_wait() {

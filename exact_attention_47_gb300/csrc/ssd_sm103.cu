@@ -1,24 +1,25 @@
 // Mamba-2 SSD forward, chunked ("Accelerating Mamba-2 with high-performance
 // forward kernels in NVIDIA CUDA Tile"): the recurrence
 //   h_t = exp(a_t) h_{t-1} + x_t b_t^T,  y_t = h_t c_t,  a_t = A[h] dt[t, h] < 0
-// evaluated chunk by chunk in the page's three kernels:
-//   1. ssd_cumsum_kernel: per chunk (restarting) running sum of a_t, scaled
-//      by log2(e) so that every later exponential is an exp2;
-//   2. ssd_state_kernel (fwd_pass_state): one CTA per (batch, head, 64-wide
-//      state tile) walks the chunks in order, storing each chunk's initial
-//      state (in bf16: the output kernel's matrix product takes it in bf16)
-//      and carrying it across the chunk in fp32 with the jump formula
-//        S <- 2^(g_last) S + sum_j 2^(g_last - g_j) x_j b_j^T
-//      (the sum is a (P x Q) * (Q x 64) contraction on the tensor cores);
-//   3. ssd_out_kernel: one CTA per (batch, chunk, head, 64-row block) forms
-//        y_i = sum_{j <= i} (c_i . b_j) 2^(g_i - g_j) x_j + 2^(g_i) S c_i
-//      as C B^T (tensor cores), the decay weights and the causal mask applied
-//      in registers, then P X and C S^T (tensor cores).
+// evaluated chunk by chunk in two tensor-core kernels (tcgen05 MMAs with fp32
+// accumulators in TMEM, operands staged in shared memory by TMA):
+//   ssd_state_kernel (the page's kernel 1 and fwd_pass_state): one CTA per
+//     (batch, pair of heads of one B/C group) walks the chunks in order.  Per
+//     chunk it forms g, the log2(e)-scaled running sum of a_t restarting at
+//     the chunk (a warp scan per head, kept in the workspace for the output
+//     kernel), stores the chunk's initial state (bf16: the output kernel's
+//     product takes it in bf16), decays the state by 2^(g_last) and adds
+//       sum_j 2^(g_last - g_j) x_j b_j^T = (x o w)^T B,
+//     one 128 x N x chunk MMA for both heads (rows = the two heads' 64
+//     columns of x, which share B), the state staying in TMEM throughout.
+//   ssd_out_kernel: one CTA per (batch, chunk, 128-row block, up to 16 heads
+//     of one group) forms C B^T once for the group's heads in TMEM; per head
+//     its entries are weighted by 2^(g_i - g_j) under the causal mask and
+//     rounded to bf16 into TMEM (P), and
+//       y_i = (P X)_i + 2^(g_i) (C S^T)_i      (S: the chunk's initial state)
+//     with P X and C S^T as MMAs and the row factor applied on the way out.
 // Every exponent is <= 0 (a_t < 0 and the mask keeps j <= i), as the page
-// notes.  Warp-level bf16 MMAs (m16n8k16, fp32 accumulation) with operands
-// staged in shared memory by cp.async, in the 128-byte-swizzled layout
-// (16-byte column c of row r at c ^ (r & 7)) that ldmatrix reads without bank
-// conflicts.  Layouts: x / y [batch, L, H, P] bf16, B / C [batch, L, G, N]
+// notes.  Layouts: x / y [batch, L, H, P] bf16, B / C [batch, L, G, N]
 // bf16, dt [batch, L, H] fp32, A [H] fp32, states [batch, H, P, N] fp32.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -30,308 +31,602 @@ namespace attn47 {
 namespace {
 
 constexpr int kP = 64;                 // head dim handled by the kernels
-constexpr int kThreads = 128;          // 4 warps
-constexpr int kNT = 64;                // state columns per ssd_state_kernel CTA
-constexpr int kIB = 64;                // query rows per ssd_out_kernel CTA
+constexpr int kHeadsPerOut = 16;       // heads of one group per output CTA
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Byte offset of 16-byte column c8 of row r in a swizzled tile of `rows`
-// rows: columns come in blocks of 64 bf16 (128-byte rows), block after block.
-__device__ __forceinline__ uint32_t swz(int rows, int r, int c8) {
-  return static_cast<uint32_t>((c8 >> 3) * rows * 128 + r * 128 + (((c8 & 7) ^ (r & 7)) << 4));
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// Copy `rows` rows of `cols` bf16 (cols a multiple of 8) from global rows
-// `row_stride` bytes apart into a swizzled tile; rows at or past `valid`
-// are zero-filled (cp.async with source size 0, given the tile's first row,
-// which the callers keep inside the tensor, as its address).  All threads of
-// the CTA take part.
-__device__ __forceinline__ void load_tile(uint32_t s_tile, const uint8_t* g0, size_t row_stride,
-                                          int rows, int cols, int valid) {
-  const int per_row = cols / 8;
-  for (int i = threadIdx.x; i < rows * per_row; i += kThreads) {
-    const int r = i / per_row, c8 = i % per_row;
-    const bool ok = r < valid;
-    const uint8_t* src = ok ? g0 + static_cast<size_t>(r) * row_stride + c8 * 16 : g0;
-    cp_async16(s_tile + swz(rows, r, c8), src, ok ? 16u : 0u);
-  }
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// ------------------------------------------------------------------ kernel 1
-__global__ void __launch_bounds__(kThreads)
-    ssd_cumsum_kernel(const float* __restrict__ dt, const float* __restrict__ A, float* __restrict__ g,
-                      int batch, int L, int H, int nc, int Q) {
-  const long long idx = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-  if (idx >= static_cast<long long>(batch) * nc * H) return;
-  const int h = static_cast<int>(idx % H);
-  const int c = static_cast<int>((idx / H) % nc);
-  const int b = static_cast<int>(idx / (static_cast<long long>(H) * nc));
-  const float a = __ldg(A + h);
-  float* out = g + ((static_cast<size_t>(b) * H + h) * nc + c) * Q;
-  float acc = 0.f;
-  for (int i = 0; i < Q; ++i) {
-    const int t = c * Q + i;
-    if (t < L) acc = fmaf(a, __ldg(dt + (static_cast<size_t>(b) * L + t) * H + h), acc);
-    out[i] = acc * kLog2e;                    // past the end: the chunk's last value
-  }
-}
-
-// ------------------------------------------------------------------ kernel 2
-struct StateSmem {
-  __host__ __device__ static constexpr int x_bytes(int Q) { return Q * kP * 2; }
-  __host__ __device__ static constexpr int b_bytes(int Q) { return Q * kNT * 2; }
+// Shared-memory layouts: every tile is rows of 128 bytes (64 bf16) in the
+// 128-byte swizzle TMA writes (8-row atoms of 1024 bytes); a tile wider than
+// 64 columns is a sequence of such 64-column chunks.
+template <int N, int Q>
+struct StateLayout {
+  static constexpr int TB = Q < 128 ? Q : 128;   // tokens per stage (one TMA box)
+  static constexpr int SPC = Q / TB;             // stages per chunk
+  static constexpr int NCH = N / 64;
+  static constexpr int kX = TB * 128;            // x of one head: TB rows x 64 columns
+  static constexpr int kB = TB * 128;            // one 64-column chunk of B
+  static constexpr int kStage = 2 * kX + NCH * kB;
+  static constexpr int kStages = 3;
+  static constexpr int kOffG = kStages * kStage; // g of the current chunk: [2][Q] fp32
+  static constexpr int kOffBar = kOffG + 2 * Q * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
 };
 
-__global__ void __launch_bounds__(kThreads)
-    ssd_state_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ Bm,
-                     const float* __restrict__ g, const float* __restrict__ h0,
-                     uint8_t* __restrict__ s_init, float* __restrict__ h_final, int L, int H, int G,
-                     int N, int nc, int Q) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+struct StateBars {
+  uint64_t full[3], empty[3], xs[3];
+  uint64_t st_ready, acc_done, mma_drain;
+  uint32_t tmem;
+  int abort;
+  int issued;                 // stages the producer started
+};
+
+struct SsdParams {
+  const float* dt;
+  const float* A;
+  const float* h0;
+  __nv_bfloat16* y;
+  float* h_final;
+  float* g;                   // workspace: [batch, H, nc, Q] fp32
+  __nv_bfloat16* s_init;      // workspace: [batch, nc, H, P, N] bf16
+  int batch, L, H, G, nc;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+// ------------------------------------------------------------ state kernel
+// Warp 0: TMA producer.  Warp 1: MMA issuer (and TMEM owner).  Warps 2-5:
+// the state's 128 rows (TMEM lane = row = head pair member * 64 + p), the
+// g scans, the stored states and the scaling of x.
+template <int N, int Q>
+__global__ void __launch_bounds__(192, 1)
+    ssd_state_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tb,
+                     const SsdParams p) {
+  using Lt = StateLayout<N, Q>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  StateBars* bar = reinterpret_cast<StateBars*>(smem + Lt::kOffBar);
+  float* gs = reinterpret_cast<float*>(smem + Lt::kOffG);
+  const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt_count = N / kNT;
-  const int n_tile = blockIdx.x % nt_count;
-  const int h = (blockIdx.x / nt_count) % H;
-  const int b = blockIdx.x / (nt_count * H);
-  const int grp = h / (H / G);
-  const int n0 = n_tile * kNT;
-  // Double-buffered chunk stages: x [Q][64], B [Q][64] (bf16, swizzled), g [Q] fp32.
-  const int stage_bytes = StateSmem::x_bytes(Q) + StateSmem::b_bytes(Q) + Q * 4;
-  const uint32_t s0 = smem_addr(smem);
-  auto sx = [&](int s) { return s0 + s * stage_bytes; };
-  auto sb = [&](int s) { return s0 + s * stage_bytes + StateSmem::x_bytes(Q); };
-  auto sg = [&](int s) {
-    return reinterpret_cast<float*>(smem + s * stage_bytes + StateSmem::x_bytes(Q) + StateSmem::b_bytes(Q));
-  };
-  const size_t x_row = static_cast<size_t>(H) * kP * 2;          // bytes between tokens of x
-  const size_t b_row = static_cast<size_t>(G) * N * 2;           // ... of B
-  const float* g_bh = g + (static_cast<size_t>(b) * H + h) * nc * Q;
-  auto issue = [&](int c, int s) {
-    const int t0 = c * Q;
-    const int valid = min(Q, L - t0);
-    load_tile(sx(s), x + ((static_cast<size_t>(b) * L + t0) * H + h) * kP * 2, x_row, Q, kP, valid);
-    load_tile(sb(s), Bm + ((static_cast<size_t>(b) * L + t0) * G + grp) * N * 2 + n0 * 2, b_row, Q, kNT, valid);
-    for (int i = threadIdx.x; i < Q / 4; i += kThreads)
-      cp_async16(smem_addr(sg(s)) + i * 16, g_bh + static_cast<size_t>(c) * Q + i * 4, 16u);
-    cp_async_commit();
-  };
 
-  // State fragment: warp w owns rows p = 16w .. 16w+15, all 64 columns
-  // (8 tiles of 16 x 8; element e of tile j at p = 16w + lane/4 + 8*(e>>1),
-  // n = 8j + 2*(lane%4) + (e&1)).
-  float S[8][4];
-  const int pr = 16 * warp + (lane >> 2);
-  const int nc2 = 2 * (lane & 3);
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int p = pr + 8 * (e >> 1), n = n0 + 8 * j + nc2 + (e & 1);
-      S[j][e] = h0 ? __ldg(h0 + ((static_cast<size_t>(b) * H + h) * kP + p) * N + n) : 0.f;
-    }
+  const int hpg = p.H / p.G;
+  const int pairs = (hpg + 1) / 2;
+  const int pair = blockIdx.x % pairs;
+  const int grp = (blockIdx.x / pairs) % p.G;
+  const int b = blockIdx.x / (pairs * p.G);
+  const int ha = grp * hpg + 2 * pair;
+  const bool has_b = 2 * pair + 1 < hpg;
+  const int hb = ha + 1;
+  const int nstage = p.nc * Lt::SPC;
 
-  issue(0, 0);
-  for (int c = 0; c < nc; ++c) {
-    const int s = c & 1;
-    if (c + 1 < nc) {
-      issue(c + 1, s ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(smem_addr(&bar->full[s]), 1);
+      mbar_init(smem_addr(&bar->empty[s]), 1);
+      mbar_init(smem_addr(&bar->xs[s]), 4);
     }
-    __syncthreads();
-    const int n_len = min(Q, L - c * Q);
-    const float* gs = sg(s);
-    const float g_last = gs[n_len - 1];
-    // x_t <- bf16(x_t * 2^(g_last - g_t)) in place (rows past the end are zero).
-    uint8_t* xs = smem + s * stage_bytes;
-    for (int i = threadIdx.x; i < Q * (kP / 8); i += kThreads) {
-      const int r = i / (kP / 8), c8 = i % (kP / 8);
-      uint4* piece = reinterpret_cast<uint4*>(xs + swz(Q, r, c8));
-      const float w = exp2f(g_last - gs[r]);
-      uint4 v = *piece;
-      uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        vw[k] = pack_bf16x2(__uint_as_float(vw[k] << 16) * w, __uint_as_float(vw[k] & 0xffff0000u) * w);
-      *piece = v;
-    }
-    // Store this chunk's initial state (bf16), then decay it to the chunk's end.
-    const float decay = exp2f(g_last);
-    uint8_t* si = s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N * 2;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int p = pr + 8 * e2, n = n0 + 8 * j + nc2;
-        *reinterpret_cast<uint32_t*>(si + (static_cast<size_t>(p) * N + n) * 2) =
-            pack_bf16x2(S[j][2 * e2], S[j][2 * e2 + 1]);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) S[j][e] *= decay;
-    }
-    fence_proxy_async_smem();                 // (generic writes above; ldmatrix reads below)
-    __syncthreads();
-    // S += (x')^T B over the chunk's Q positions: A[p][t] from x' [t][p]
-    // (transposed load), B[t][n] from B [t][n] (transposed load).
-    const uint32_t ax = sx(s), bx = sb(s);
-    for (int kk = 0; kk < Q / 16; ++kk) {
-      uint32_t a[4];
-      {
-        const int t = 16 * kk + (lane & 7) + ((lane >> 4) << 3);
-        const int c8 = 2 * warp + ((lane >> 3) & 1);
-        ldsm_x4_trans(ax + swz(Q, t, c8), a);
-      }
-#pragma unroll
-      for (int j2 = 0; j2 < 4; ++j2) {
-        const int t = 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c8 = 2 * j2 + (lane >> 4);
-        uint32_t bb[4];
-        ldsm_x4_trans(bx + swz(Q, t, c8), bb);
-        mma_16816(S[2 * j2], a, bb[0], bb[1]);
-        mma_16816(S[2 * j2 + 1], a, bb[2], bb[3]);
-      }
-    }
-    __syncthreads();                          // the stage is refilled two chunks later
+    mbar_init(smem_addr(&bar->st_ready), 4);
+    mbar_init(smem_addr(&bar->acc_done), 1);
+    mbar_init(smem_addr(&bar->mma_drain), 1);
+    bar->abort = 0;
+    bar->issued = 0;
+    fence_mbar_init();
   }
-  float* hf = h_final + (static_cast<size_t>(b) * H + h) * kP * N;
+  if (!has_b) {
+    // The second head's rows of x stay zero (it is never loaded).
+    for (int s = 0; s < 3; ++s)
+      for (int i = threadIdx.x; i < Lt::kX / 16; i += blockDim.x)
+        *reinterpret_cast<uint4*>(smem + s * Lt::kStage + Lt::kX + i * 16) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&bar->tmem), N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem;
+  const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t bytes = (has_b ? 2 : 1) * Lt::kX + Lt::NCH * Lt::kB;
+      for (int s = 0; s < nstage; ++s) {
+        const int st = s % 3;
+        if (!mbar_wait(smem_addr(&bar->empty[st]), ((s / 3) & 1) ^ 1, wc)) break;
+        bar->issued = s + 1;
+        const int t = (s / Lt::SPC) * Q + (s % Lt::SPC) * Lt::TB;
+        const uint32_t fb = smem_addr(&bar->full[st]);
+        const uint32_t dst = sbase + st * Lt::kStage;
+        mbar_arrive_expect_tx(fb, bytes);
+        tma_load_4d(dst, &tx, fb, 0, ha, t, b);
+        if (has_b) tma_load_4d(dst + Lt::kX, &tx, fb, 0, hb, t, b);
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      const int p = pr + 8 * e2, n = n0 + 8 * j + nc2;
-      *reinterpret_cast<float2*>(hf + static_cast<size_t>(p) * N + n) = make_float2(S[j][2 * e2], S[j][2 * e2 + 1]);
+        for (int ch = 0; ch < Lt::NCH; ++ch) tma_load_4d(dst + 2 * Lt::kX + ch * Lt::kB, &tb, fb, 64 * ch, grp, t, b);
+      }
     }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdesc = idesc_bf16_f32_ab(128, N, true, true);
+    for (int c = 0; c < p.nc; ++c) {
+      if (!mbar_wait_warp(smem_addr(&bar->st_ready), c & 1, wc)) break;
+      tc_fence_after();
+      bool ok = true;
+      for (int k = 0; k < Lt::SPC; ++k) {
+        const int s = c * Lt::SPC + k;
+        const int st = s % 3;
+        if (!mbar_wait_warp(smem_addr(&bar->xs[st]), (s / 3) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t xa = sbase + st * Lt::kStage;
+        const uint32_t bb = xa + 2 * Lt::kX;
+        // D (rows: the two heads' x columns, cols: n) += x'^T B over the
+        // stage's tokens.  A and B are stored token-major (M and N contiguous).
+#pragma unroll
+        for (int kk = 0; kk < Lt::TB / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(xa + kk * 2048, Lt::kX, 1024);
+          const uint64_t bd = sdesc_sw128(bb + kk * 2048, Lt::kB, 1024);
+          umma_ss_warp(tmem, ad, bd, kIdesc, 1u);
+        }
+        umma_commit_warp(smem_addr(&bar->empty[st]));
+      }
+      if (!ok) break;
+      umma_commit_warp(smem_addr(&bar->acc_done));
+    }
+    // Every MMA this warp issued completes before TMEM is released.
+    umma_commit_warp(smem_addr(&bar->mma_drain));
+    mbar_wait_warp_drain(smem_addr(&bar->mma_drain), 0, wc);
+  } else {
+    // ------------------------------------------------------------- rows
+    const int tid = threadIdx.x - 64;          // 0 .. 127
+    const int wq = warp & 3;                   // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;              // state row
+    const int sel = r >> 6;
+    const int pr = r & 63;
+    const int hrow = sel ? hb : ha;
+    const bool vrow = sel == 0 || has_b;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    // Initial state: h0 or zero.
+#pragma unroll 1
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float x = 0.f;
+        if (p.h0 != nullptr && vrow) x = __ldg(p.h0 + ((static_cast<size_t>(b) * p.H + hrow) * kP + pr) * N + c0 + i);
+        v[i] = __float_as_uint(x);
+      }
+      ATTN47_TMEM_ST32(trow + c0, v);
+    }
+    tmem_st_wait();
+    // The four warps meet at two named barriers per chunk.  A warp whose
+    // wait gave up skips the rest of its chunk but still reaches both
+    // barriers; at the first one of the next chunk they all learn of it and
+    // leave together (no warp is left waiting at a barrier).
+    bool ok = true;
+    for (int c = 0; c < p.nc; ++c) {
+      const int t0 = c * Q;
+      const int n_len = min(Q, p.L - t0);
+      // Every row is done with the previous chunk's g.
+      if (named_barrier_or(1, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      // g of the chunk: warp 2 for head a, warp 3 for head b.  Past the end of
+      // the sequence a_t counts as 0, so g keeps the chunk's last value.
+      if (warp == 2 || (warp == 3 && has_b)) {
+        const int h = warp == 2 ? ha : hb;
+        const float a = __ldg(p.A + h);
+        constexpr int E = Q / 32;
+        float v[E];
+        float run = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const int i = lane * E + e;
+          const float d = i < n_len ? __ldg(p.dt + (static_cast<size_t>(b) * p.L + t0 + i) * p.H + h) : 0.f;
+          run = fmaf(a, d, run);
+          v[e] = run;
+        }
+        float incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const float offset = incl - run;
+        float* gw = p.g + ((static_cast<size_t>(b) * p.H + h) * p.nc + c) * Q;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float gv = (v[e] + offset) * kLog2e;
+          gs[(warp - 2) * Q + lane * E + e] = gv;
+          gw[lane * E + e] = gv;
+        }
+      }
+      named_barrier_sync(1, 128);
+      // x_t <- bf16(x_t * 2^(g_last - g_t)) in place, stage by stage (rows
+      // past the sequence end are zero and stay zero).
+      for (int k = 0; k < Lt::SPC; ++k) {
+        const int s = c * Lt::SPC + k;
+        const int st = s % 3;
+        if (!mbar_wait_warp(smem_addr(&bar->full[st]), (s / 3) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        uint8_t* xs = smem + st * Lt::kStage;
+        for (int q = tid; q < (has_b ? 2 : 1) * Lt::TB * 8; q += 128) {
+          const int hs = q / (Lt::TB * 8);
+          const int row = (q >> 3) % Lt::TB;
+          const int tt = k * Lt::TB + row;
+          const float w = tt < n_len ? ex2(gs[hs * Q + Q - 1] - gs[hs * Q + tt]) : 0.f;
+          uint4* piece = reinterpret_cast<uint4*>(xs + hs * Lt::kX + row * 128 + (q & 7) * 16);
+          uint4 v = *piece;
+          uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            vw[e] = pack_bf16x2(__uint_as_float(vw[e] << 16) * w, __uint_as_float(vw[e] & 0xffff0000u) * w);
+          *piece = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bar->xs[st]));
+      }
+      // The chunk's initial state (once the previous chunk's MMAs are
+      // complete) is stored, then decayed to the chunk's end in place.  The
+      // scaling above overlaps with those MMAs.
+      if (!ok) continue;
+      if (c > 0 && !mbar_wait_warp(smem_addr(&bar->acc_done), (c - 1) & 1, wc)) {
+        ok = false;
+        continue;
+      }
+      tc_fence_after();
+      const float decay = vrow ? ex2(gs[sel * Q + Q - 1]) : 0.f;
+      __nv_bfloat16* si = p.s_init + ((static_cast<size_t>(b) * p.nc + c) * p.H + hrow) * kP * N + pr * N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t v[32];
+        ATTN47_TMEM_LD32(trow + c0, v);
+        ATTN47_TMEM_LD_WAIT(v);
+        if (vrow) {
+          uint4* dst = reinterpret_cast<uint4*>(si + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * decay);
+        ATTN47_TMEM_ST32(trow + c0, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->st_ready));
+    }
+    // Final state.
+    if (ok && mbar_wait_warp(smem_addr(&bar->acc_done), (p.nc - 1) & 1, wc)) {
+      tc_fence_after();
+      float* hf = p.h_final + ((static_cast<size_t>(b) * p.H + hrow) * kP + pr) * N;
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t v[32];
+        ATTN47_TMEM_LD32(trow + c0, v);
+        ATTN47_TMEM_LD_WAIT(v);
+        if (vrow) {
+          float4* dst = reinterpret_cast<float4*>(hf + c0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+    }
+  }
+  // Copies still in flight (a CTA that gave up early) must land first.
+  if (warp == 0 && lane == 0) {
+    const int issued = bar->issued;
+    for (int st = 0; st < 3 && st < issued; ++st) {
+      const int fills = (issued - 1 - st) / 3 + 1;
+      mbar_wait(smem_addr(&bar->full[st]), (fills - 1) & 1, wc, true);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, N);
+  }
 }
 
-// ------------------------------------------------------------------ kernel 3
-template <int N>
-__global__ void __launch_bounds__(kThreads)
-    ssd_out_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ Bm,
-                   const uint8_t* __restrict__ Cm, const float* __restrict__ g,
-                   const uint8_t* __restrict__ s_init, uint8_t* __restrict__ y, int L, int H, int G,
-                   int nc, int Q) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+// ----------------------------------------------------------- output kernel
+template <int N, int Q>
+struct OutLayout {
+  static constexpr int TB = Q < 128 ? Q : 128;   // rows of one TMA box
+  static constexpr int NCH = N / 64;
+  static constexpr int kC = 128 * 128;           // one 64-column chunk of the C block (128 rows)
+  static constexpr int kBch = Q * 128;           // one 64-column chunk of B (up to Q keys)
+  static constexpr int kX = Q * 128;             // X of one head (up to Q keys x 64)
+  static constexpr int kS = 64 * 128;            // one 64-column chunk of S (64 rows)
+  static constexpr int kOffC = 0;
+  static constexpr int kOffB = kOffC + NCH * kC;
+  static constexpr int kOffX = kOffB + NCH * kBch;
+  static constexpr int kOffS = kOffX + 2 * kX;
+  static constexpr int kOffG = kOffS + 2 * NCH * kS;
+  static constexpr int kOffBar = kOffG + 2 * Q * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;
+  // TMEM columns: C B^T, P (bf16 pairs), P X, C S^T.
+  static constexpr uint32_t kColCB = 0, kColP = 256, kColY = 384, kColYc = 448;
+};
+
+struct OutBars {
+  uint64_t cb_full, cb_done;
+  uint64_t xf[2], xe[2];
+  uint64_t p_full, y_full, y_free, mma_drain;
+  uint32_t tmem;
+  int abort;
+  int issued;                 // heads whose operands the producer started
+};
+
+// Warp 0: TMA producer.  Warp 1: MMA issuer (and TMEM owner).  Warps 2-9:
+// two per TMEM lane quarter (row = lane), each taking half of the keys (P)
+// and half of the 64 output columns (epilogue).
+template <int N, int Q>
+__global__ void __launch_bounds__(320, 1)
+    ssd_out_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tb,
+                   const __grid_constant__ CUtensorMap tc, const __grid_constant__ CUtensorMap ts,
+                   const SsdParams p) {
+  using Lt = OutLayout<N, Q>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  OutBars* bar = reinterpret_cast<OutBars*>(smem + Lt::kOffBar);
+  const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_ib = Q / kIB;
-  const int ib = blockIdx.x % n_ib;
-  const int h = (blockIdx.x / n_ib) % H;
-  const int c = (blockIdx.x / (n_ib * H)) % nc;
-  const int b = blockIdx.x / (n_ib * H * nc);
-  const int grp = h / (H / G);
+
+  const int hpg = p.H / p.G;
+  const int ngrp = (hpg + kHeadsPerOut - 1) / kHeadsPerOut;
+  const int nrb = (Q + 127) / 128;
+  int idx = blockIdx.x;
+  const int hgi = idx % ngrp;
+  idx /= ngrp;
+  const int grp = idx % p.G;
+  idx /= p.G;
+  const int rb = idx % nrb;
+  idx /= nrb;
+  const int c = idx % p.nc;
+  const int b = idx / p.nc;
+  const int h0 = grp * hpg + hgi * kHeadsPerOut;
+  const int nh = min(kHeadsPerOut, hpg - hgi * kHeadsPerOut);
   const int t0 = c * Q;
-  const int n_len = min(Q, L - t0);
-  if (ib * kIB >= n_len) return;              // a block wholly past the end writes nothing
-  const int jrows = kIB * (ib + 1);           // keys 0 .. 64(ib+1)-1 of the chunk
-  // Shared memory: C_i [64][N], B [jrows][N], X [jrows][64], S [64][N] (bf16,
-  // swizzled), g [Q] fp32.
-  const uint32_t s0 = smem_addr(smem);
-  const uint32_t sC = s0;
-  const uint32_t sB = sC + kIB * N * 2;
-  const uint32_t sX = sB + jrows * N * 2;
-  const uint32_t sS = sX + jrows * kP * 2;
-  float* gs = reinterpret_cast<float*>(smem + (sS - s0) + kP * N * 2);
-  const size_t bc_row = static_cast<size_t>(G) * N * 2;
-  const uint8_t* c0 = Cm + ((static_cast<size_t>(b) * L + t0 + ib * kIB) * G + grp) * N * 2;
-  load_tile(sC, c0, bc_row, kIB, N, n_len - ib * kIB);
-  load_tile(sB, Bm + ((static_cast<size_t>(b) * L + t0) * G + grp) * N * 2, bc_row, jrows, N, n_len);
-  load_tile(sX, x + ((static_cast<size_t>(b) * L + t0) * H + h) * kP * 2, static_cast<size_t>(H) * kP * 2,
-            jrows, kP, n_len);
-  // The chunk's initial state S [p][n] (bf16, as the state kernel stored it).
-  load_tile(sS, s_init + ((static_cast<size_t>(b) * nc + c) * H + h) * kP * N * 2,
-            static_cast<size_t>(N) * 2, kP, N, kP);
-  const float* g_c = g + ((static_cast<size_t>(b) * H + h) * nc + c) * Q;
-  for (int i = threadIdx.x; i < Q / 4; i += kThreads) cp_async16(smem_addr(gs) + i * 16, g_c + i * 4, 16u);
-  cp_async_commit();
-  cp_async_wait<0>();
+  const int n_len = min(Q, p.L - t0);
+  const int J = min(Q, 128 * (rb + 1));          // keys 0 .. J-1 of the chunk
+  const int kb_count = J / Lt::TB;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar->cb_full), 1);
+    mbar_init(smem_addr(&bar->cb_done), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&bar->xf[s]), 1);
+      mbar_init(smem_addr(&bar->xe[s]), 1);
+    }
+    mbar_init(smem_addr(&bar->p_full), 8);
+    mbar_init(smem_addr(&bar->y_full), 1);
+    mbar_init(smem_addr(&bar->y_free), 8);
+    mbar_init(smem_addr(&bar->mma_drain), 1);
+    bar->abort = 0;
+    bar->issued = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&bar->tmem), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem;
+  const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
 
-  // Rows of this warp: i = ib*64 + 16*warp + lane/4 (+8); A fragments of C_i
-  // for the N/16 steps of the contraction over the state dimension.
-  uint32_t ca[N / 16][4];
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t fb = smem_addr(&bar->cb_full);
+      mbar_arrive_expect_tx(fb, Lt::NCH * Lt::kC + Lt::NCH * J * 128);
 #pragma unroll
-  for (int kk = 0; kk < N / 16; ++kk)
-    ldsm_x4(sC + swz(kIB, 16 * warp + (lane & 15), 2 * kk + (lane >> 4)), ca[kk]);
-  const int il0 = ib * kIB + 16 * warp + (lane >> 2);              // chunk position of rows e = 0, 1
-  const float gi0 = gs[min(il0, Q - 1)], gi1 = gs[min(il0 + 8, Q - 1)];
+      for (int ch = 0; ch < Lt::NCH; ++ch) {
+        tma_load_4d(sbase + Lt::kOffC + ch * Lt::kC, &tc, fb, 64 * ch, grp, t0 + rb * 128, b);
+        for (int kb = 0; kb < kb_count; ++kb)
+          tma_load_4d(sbase + Lt::kOffB + ch * Lt::kBch + kb * Lt::TB * 128, &tb, fb, 64 * ch, grp,
+                      t0 + kb * Lt::TB, b);
+      }
+      for (int k = 0; k < nh; ++k) {
+        const int st = k & 1;
+        if (!mbar_wait(smem_addr(&bar->xe[st]), ((k >> 1) & 1) ^ 1, wc)) break;
+        bar->issued = k + 1;
+        const int h = h0 + k;
+        const uint32_t xb = smem_addr(&bar->xf[st]);
+        mbar_arrive_expect_tx(xb, J * 128 + Lt::NCH * Lt::kS + Q * 4);
+        for (int kb = 0; kb < kb_count; ++kb)
+          tma_load_4d(sbase + Lt::kOffX + st * Lt::kX + kb * Lt::TB * 128, &tx, xb, 0, h, t0 + kb * Lt::TB, b);
+        const int srow = ((b * p.nc + c) * p.H + h) * kP;
+#pragma unroll
+        for (int ch = 0; ch < Lt::NCH; ++ch)
+          tma_load_2d(sbase + Lt::kOffS + (st * Lt::NCH + ch) * Lt::kS, &ts, xb, 64 * ch, srow);
+        bulk_load(sbase + Lt::kOffG + st * Q * 4, p.g + ((static_cast<size_t>(b) * p.H + h) * p.nc + c) * Q,
+                  Q * 4, xb);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------- MMA issuer
+    bool ok = mbar_wait_warp(smem_addr(&bar->cb_full), 0, wc);
+    if (ok) {
+      tc_fence_after();
+      // C B^T: A = C (rows i, K = n), B = B (rows j, K = n), both K-major.
+      const uint32_t idesc = idesc_bf16_f32_ab(128, J, false, false);
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(sbase + Lt::kOffC + (kk >> 2) * Lt::kC + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(sbase + Lt::kOffB + (kk >> 2) * Lt::kBch + (kk & 3) * 32, 16, 1024);
+        umma_ss_warp(tmem + Lt::kColCB, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(smem_addr(&bar->cb_done));
+    }
+    constexpr uint32_t kIdescPX = idesc_bf16_f32_ab(128, 64, false, true);
+    constexpr uint32_t kIdescCS = idesc_bf16_f32_ab(128, 64, false, false);
+    for (int k = 0; k < nh && ok; ++k) {
+      const int st = k & 1;
+      ok = mbar_wait_warp(smem_addr(&bar->xf[st]), (k >> 1) & 1, wc) &&
+           mbar_wait_warp(smem_addr(&bar->p_full), k & 1, wc) &&
+           mbar_wait_warp(smem_addr(&bar->y_free), (k & 1) ^ 1, wc);
+      if (!ok) break;
+      tc_fence_after();
+      // P X: A = P from TMEM (8 columns = 16 keys per step), B = X (keys x
+      // 64, column-contiguous: MN-major).
+      for (int kk = 0; kk < J / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(sbase + Lt::kOffX + st * Lt::kX + kk * 2048, Lt::kX, 1024);
+        umma_ts_warp(tmem + Lt::kColY, tmem + Lt::kColP + kk * 8, bd, kIdescPX, kk > 0 ? 1u : 0u);
+      }
+      // C S^T: A = C, B = S (rows p, K = n): both K-major.
+#pragma unroll
+      for (int kk = 0; kk < N / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(sbase + Lt::kOffC + (kk >> 2) * Lt::kC + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd =
+            sdesc_sw128(sbase + Lt::kOffS + (st * Lt::NCH + (kk >> 2)) * Lt::kS + (kk & 3) * 32, 16, 1024);
+        umma_ss_warp(tmem + Lt::kColYc, ad, bd, kIdescCS, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(smem_addr(&bar->y_full));
+      umma_commit_warp(smem_addr(&bar->xe[st]));
+    }
+    umma_commit_warp(smem_addr(&bar->mma_drain));
+    mbar_wait_warp_drain(smem_addr(&bar->mma_drain), 0, wc);
+  } else {
+    // ------------------------------------------------------------- rows
+    const int wq = warp & 3;
+    const int hf = (warp - 2) >> 2;            // half of the keys / of the output columns
+    const int r = wq * 32 + lane;
+    const int i_abs = rb * 128 + r;            // row's position in the chunk
+    const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float* gsm_base = reinterpret_cast<const float*>(smem + Lt::kOffG);
+    auto epilogue = [&](int k, float gi) {
+      uint32_t yv[32], cv[32];
+      ATTN47_TMEM_LD32(trow + Lt::kColY + hf * 32, yv);
+      ATTN47_TMEM_LD32(trow + Lt::kColYc + hf * 32, cv);
+      ATTN47_TMEM_LD_WAIT(yv);
+      ATTN47_TMEM_LD_WAIT(cv);
+      if (i_abs < n_len) {
+        const float w = ex2(gi);
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.y + ((static_cast<size_t>(b) * p.L + t0 + i_abs) * p.H + h0 + k) * kP + hf * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 8 * q + 2 * e;
+            o[e] = pack_bf16x2(fmaf(w, __uint_as_float(cv[cc]), __uint_as_float(yv[cc])),
+                               fmaf(w, __uint_as_float(cv[cc + 1]), __uint_as_float(yv[cc + 1])));
+          }
+          dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->y_free));
+    };
+    bool ok = mbar_wait_warp(smem_addr(&bar->cb_done), 0, wc);
+    tc_fence_after();
+    float g_prev = 0.f;
+    int k = 0;
+    for (; k < nh && ok; ++k) {
+      const int st = k & 1;
+      if (!mbar_wait_warp(smem_addr(&bar->xf[st]), (k >> 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
+      if (k > 0) {
+        if (!mbar_wait_warp(smem_addr(&bar->y_full), (k - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        epilogue(k - 1, g_prev);
+      }
+      // P = (C B^T) o 2^(g_i - g_j) under the causal mask, this warp's half
+      // of the keys, 32 at a time (16 bf16 pairs per TMEM column group).
+      const float* gsm = gsm_base + st * Q;
+      const float gi = gsm[min(i_abs, Q - 1)];
+      const int j0 = hf * (J >> 1);
+      for (int jg = 0; jg < (J >> 1); jg += 32) {
+        uint32_t v[32];
+        ATTN47_TMEM_LD32(trow + Lt::kColCB + j0 + jg, v);
+        ATTN47_TMEM_LD_WAIT(v);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = j0 + jg + 2 * e;
+          const float p0 = j <= i_abs ? __uint_as_float(v[2 * e]) * ex2(gi - gsm[j]) : 0.f;
+          const float p1 = j + 1 <= i_abs ? __uint_as_float(v[2 * e + 1]) * ex2(gi - gsm[j + 1]) : 0.f;
+          w[e] = pack_bf16x2(p0, p1);
+        }
+        ATTN47_TMEM_ST16(trow + Lt::kColP + ((j0 + jg) >> 1), w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+      g_prev = gi;
+    }
+    if (ok && nh > 0 && mbar_wait_warp(smem_addr(&bar->y_full), (nh - 1) & 1, wc)) {
+      tc_fence_after();
+      epilogue(nh - 1, g_prev);
+    }
+  }
+  // Copies still in flight (a CTA that gave up early) must land first.
+  if (warp == 0 && lane == 0) {
+    mbar_wait(smem_addr(&bar->cb_full), 0, wc, true);
+    const int issued = bar->issued;
+    for (int st = 0; st < 2 && st < issued; ++st) {
+      const int fills = (issued - 1 - st) / 2 + 1;
+      mbar_wait(smem_addr(&bar->xf[st]), (fills - 1) & 1, wc, true);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
 
-  float Y[8][4], Yc[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) Y[j][e] = Yc[j][e] = 0.f;
-  // Within the chunk: for each 64-key block, S = C_i B_j^T, weights and mask,
-  // then Y += P X_j.
-  for (int jb = 0; jb <= ib; ++jb) {
-    float sc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      const int key = jb * kIB + nt * 8 + (lane & 7);
-#pragma unroll
-      for (int kk2 = 0; kk2 < N / 32; ++kk2) {
-        uint32_t bb[4];
-        ldsm_x4(sB + swz(jrows, key, 4 * kk2 + (lane >> 3)), bb);
-        mma_16816(sc[nt], ca[2 * kk2], bb[0], bb[1]);
-        mma_16816(sc[nt], ca[2 * kk2 + 1], bb[2], bb[3]);
-      }
-    }
-    uint32_t pa[4][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      float v[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = il0 + 8 * (e >> 1);
-        const int j = jb * kIB + nt * 8 + 2 * (lane & 3) + (e & 1);
-        const float gi = (e >> 1) ? gi1 : gi0;
-        v[e] = (j <= i) ? sc[nt][e] * exp2f(gi - gs[j]) : 0.f;
-      }
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(v[0], v[1]);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(v[2], v[3]);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dt2 = 0; dt2 < kP / 16; ++dt2) {
-        const int key = jb * kIB + 16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8;
-        uint32_t bb[4];
-        ldsm_x4_trans(sX + swz(jrows, key, 2 * dt2 + (lane >> 4)), bb);
-        mma_16816(Y[2 * dt2], pa[kk], bb[0], bb[1]);
-        mma_16816(Y[2 * dt2 + 1], pa[kk], bb[2], bb[3]);
-      }
-    }
-  }
-  // Carried state: Yc = C_i S^T  (B operand rows = p, columns = n).
-#pragma unroll
-  for (int pt = 0; pt < 8; ++pt) {
-#pragma unroll
-    for (int kk2 = 0; kk2 < N / 32; ++kk2) {
-      uint32_t bb[4];
-      ldsm_x4(sS + swz(kP, 8 * pt + (lane & 7), 4 * kk2 + (lane >> 3)), bb);
-      mma_16816(Yc[pt], ca[2 * kk2], bb[0], bb[1]);
-      mma_16816(Yc[pt], ca[2 * kk2 + 1], bb[2], bb[3]);
-    }
-  }
-  // y_i = Y_i + 2^(g_i) Yc_i, rows past the end of the sequence skipped.
-  const float w0 = exp2f(gi0), w1 = exp2f(gi1);
-#pragma unroll
-  for (int e2 = 0; e2 < 2; ++e2) {
-    const int i = il0 + 8 * e2;
-    if (i >= n_len) continue;
-    const float w = e2 ? w1 : w0;
-    uint8_t* yrow = y + ((static_cast<size_t>(b) * L + t0 + i) * H + h) * kP * 2;
-#pragma unroll
-    for (int pt = 0; pt < 8; ++pt) {
-      const int p = 8 * pt + 2 * (lane & 3);
-      *reinterpret_cast<uint32_t*>(yrow + p * 2) =
-          pack_bf16x2(Y[pt][2 * e2] + w * Yc[pt][2 * e2], Y[pt][2 * e2 + 1] + w * Yc[pt][2 * e2 + 1]);
-    }
-  }
+template <int N, int Q>
+cudaError_t launch_nq(const SsdLaunch& a, const SsdParams& p) {
+  using Ls = StateLayout<N, Q>;
+  using Lo = OutLayout<N, Q>;
+  auto ks = ssd_state_kernel<N, Q>;
+  auto ko = ssd_out_kernel<N, Q>;
+  // The output kernel takes all 512 TMEM columns: its shared memory is
+  // padded so that one CTA fits per SM.
+  constexpr int kOutSmem = Lo::kSmem > 120 * 1024 ? Lo::kSmem : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, Ls::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, kOutSmem);
+  if (e != cudaSuccess) return e;
+  const int hpg = a.H / a.G;
+  const long long grid1 = static_cast<long long>(a.batch) * a.G * ((hpg + 1) / 2);
+  ks<<<static_cast<unsigned>(grid1), 192, Ls::kSmem, a.stream>>>(*a.tx, *a.tb, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long grid2 = static_cast<long long>(a.batch) * p.nc * ((Q + 127) / 128) * a.G *
+                          ((hpg + kHeadsPerOut - 1) / kHeadsPerOut);
+  ko<<<static_cast<unsigned>(grid2), 320, kOutSmem, a.stream>>>(*a.tx, *a.tb, *a.tc, *a.ts, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -345,36 +640,37 @@ size_t ssd_workspace_bytes(int batch, int L, int H, int N, int chunk) {
 
 int ssd_head_dim() { return kP; }
 
+size_t ssd_states_offset(int batch, int L, int H, int chunk) {
+  const size_t nc = (static_cast<size_t>(L) + chunk - 1) / chunk;
+  const size_t g_bytes = static_cast<size_t>(batch) * H * nc * chunk * 4;
+  return (g_bytes + 255) & ~static_cast<size_t>(255);
+}
+
 cudaError_t launch_ssd_sm103(const SsdLaunch& a) {
-  const int nc = (a.L + a.chunk - 1) / a.chunk;
-  const size_t g_bytes = static_cast<size_t>(a.batch) * a.H * nc * a.chunk * 4;
-  float* g = static_cast<float*>(a.workspace);
-  uint8_t* s_init = static_cast<uint8_t*>(a.workspace) + ((g_bytes + 255) & ~static_cast<size_t>(255));
-  const long long n1 = static_cast<long long>(a.batch) * nc * a.H;
-  ssd_cumsum_kernel<<<static_cast<unsigned>((n1 + kThreads - 1) / kThreads), kThreads, 0, a.stream>>>(
-      a.dt, a.A, g, a.batch, a.L, a.H, nc, a.chunk);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  const int smem2 = 2 * (StateSmem::x_bytes(a.chunk) + StateSmem::b_bytes(a.chunk) + a.chunk * 4);
-  e = cudaFuncSetAttribute(ssd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem2);
-  if (e != cudaSuccess) return e;
-  const unsigned grid2 = static_cast<unsigned>(static_cast<long long>(a.batch) * a.H * (a.N / kNT));
-  ssd_state_kernel<<<grid2, kThreads, smem2, a.stream>>>(
-      static_cast<const uint8_t*>(a.x), static_cast<const uint8_t*>(a.B), g, a.h0, s_init, a.h_final,
-      a.L, a.H, a.G, a.N, nc, a.chunk);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  const int smem3 = kIB * a.N * 2 + a.chunk * a.N * 2 + a.chunk * kP * 2 + kP * a.N * 2 + a.chunk * 4;
-  const unsigned grid3 = static_cast<unsigned>(static_cast<long long>(a.batch) * nc * a.H * (a.chunk / kIB));
-  auto k3 = a.N == 128 ? ssd_out_kernel<128> : ssd_out_kernel<64>;
-  e = cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, smem3);
-  if (e != cudaSuccess) return e;
-  k3<<<grid3, kThreads, smem3, a.stream>>>(static_cast<const uint8_t*>(a.x), static_cast<const uint8_t*>(a.B),
-                                           static_cast<const uint8_t*>(a.C), g, s_init,
-                                           static_cast<uint8_t*>(a.y), a.L, a.H, a.G, nc, a.chunk);
-  return cudaGetLastError();
+  SsdParams p;
+  p.dt = a.dt;
+  p.A = a.A;
+  p.h0 = a.h0;
+  p.y = static_cast<__nv_bfloat16*>(a.y);
+  p.h_final = a.h_final;
+  p.g = static_cast<float*>(a.workspace);
+  p.s_init = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(a.workspace) +
+                                              ssd_states_offset(a.batch, a.L, a.H, a.chunk));
+  p.batch = a.batch;
+  p.L = a.L;
+  p.H = a.H;
+  p.G = a.G;
+  p.nc = (a.L + a.chunk - 1) / a.chunk;
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  if (a.N == 128) {
+    if (a.chunk == 256) return launch_nq<128, 256>(a, p);
+    if (a.chunk == 128) return launch_nq<128, 128>(a, p);
+    return launch_nq<128, 64>(a, p);
+  }
+  if (a.chunk == 256) return launch_nq<64, 256>(a, p);
+  if (a.chunk == 128) return launch_nq<64, 128>(a, p);
+  return launch_nq<64, 64>(a, p);
 }
 
 }  // namespace attn47

@@ -333,11 +333,12 @@ size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk);
  * Tile": per (batch, head), with a_t = A[h] * dt[t, h] (< 0) and state
  * h_t of size P x N,
  *   h_t = exp(a_t) h_{t-1} + x_t b_t^T,   y_t = h_t c_t,
- * evaluated chunk by chunk with the page's three kernels: the per-chunk
- * cumulative sum of a_t scaled by log2(e); fwd_pass_state, a sequential loop
- * over chunks that gives every chunk's initial state and the final state;
- * and the chunk outputs (C B^T weighted by exp(g_i - g_j) under the causal
- * mask, times X, plus the initial state's contribution).  x enters the
+ * evaluated chunk by chunk: the page's per-chunk cumulative sum of a_t
+ * (scaled by log2(e)) and fwd_pass_state, the sequential loop over chunks
+ * that gives every chunk's initial state and the final state, run as one
+ * kernel; the chunk outputs (C B^T weighted by exp(g_i - g_j) under the
+ * causal mask, times X, plus the initial state's contribution) as a second.
+ * Both do their matrix products on the tensor cores.  x enters the
  * recurrence as given (pass x * dt for Mamba-2's discretised input).
  *
  *  x        [batch, L, H, P] bf16;  dt [batch, L, H] fp32 (> 0);  A [H] fp32 (< 0)
@@ -350,7 +351,8 @@ size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk);
  *  P must be 64; N 64 or 128; chunk 64, 128 or 256; H % G == 0.  bf16 and
  *  state pointers 16-byte aligned, dt and A 4-byte aligned.
  *  batch == 0 or L == 0 is an empty problem: ATTN_OK, nothing launched.
- *  Launches three kernels in stream order.  Deterministic.
+ *  Launches two kernels in stream order.  Deterministic.  Calls that share a
+ *  workspace must not overlap.
  */
 attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, const void* B,
                               const void* C, const float* h0, void* y, float* h_final, int batch,

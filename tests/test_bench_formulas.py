@@ -54,18 +54,19 @@ def test_fusion_byte_counts():
 
 
 def test_ssd_flops_counts_the_matrix_form():
-    # Per (batch, head) and chunk of n positions: the masked C B^T and its
-    # product with X over n^2/2 pairs (N and P multiply-adds each), the
-    # state update and the carried state's output (P N multiply-adds per
-    # position each).
-    batch, L, H, P, N, chunk = 2, 300, 3, 8, 16, 128
+    # Per chunk of n positions: the masked C B^T once per B/C group (n^2/2
+    # pairs of N multiply-adds), and per head its product with X over the
+    # same pairs (P multiply-adds each), the state update and the carried
+    # state's output (P N multiply-adds per position each).
+    batch, L, H, G, P, N, chunk = 2, 300, 6, 2, 8, 16, 128
     total = 0
     for c0 in range(0, L, chunk):
         n = min(chunk, L - c0)
         pairs = n * n / 2
-        total += pairs * 2 * N + pairs * 2 * P      # C B^T, then (.) X
-        total += n * 2 * P * N + n * 2 * P * N      # (x w)^T B, C S^T
-    assert bench.ssd_flops(batch, L, H, P, N, chunk) == batch * H * total
+        total += G * pairs * 2 * N                       # C B^T per group
+        total += H * pairs * 2 * P                       # (.) X per head
+        total += H * (n * 2 * P * N + n * 2 * P * N)     # (x w)^T B, C S^T per head
+    assert bench.ssd_flops(batch, L, H, G, P, N, chunk) == batch * total
 
 
 def test_ssd_bytes_lists_every_tensor():

@@ -37,6 +37,9 @@ def _run(d, chunk, h0=None):
 CASES = [  # batch, L, H, G, N, chunk, with h0
     (1, 64, 2, 1, 64, 64, False), (2, 200, 4, 2, 128, 64, False), (1, 300, 3, 1, 128, 128, True),
     (1, 512, 2, 1, 64, 256, True), (1, 1, 2, 1, 64, 64, False), (2, 777, 2, 1, 128, 256, True),
+    # more than 16 heads per group (two output blocks, the second partial),
+    # an odd number of heads per group, several groups
+    (1, 300, 20, 1, 128, 256, False), (1, 129, 5, 1, 64, 128, False), (2, 130, 8, 2, 64, 128, True),
 ]
 
 
