@@ -780,7 +780,7 @@ attn_status_t ssd_chunked_fwd(const void* x, const float* dt, const float* A, co
   // the bf16 chunk states in the workspace over (N, batch * nc * H * P).
   CUtensorMap tx, tb, tc, ts;
   {
-    const cuuint32_t rows = static_cast<cuuint32_t>(chunk < 128 ? chunk : 128);
+    const cuuint32_t rows = 64;
     const cuuint64_t xdims[4] = {static_cast<cuuint64_t>(P), static_cast<cuuint64_t>(H),
                                  static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(batch)};
     const cuuint64_t xstr[3] = {static_cast<cuuint64_t>(P) * 2, static_cast<cuuint64_t>(H) * P * 2,

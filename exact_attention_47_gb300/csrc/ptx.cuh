@@ -109,6 +109,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to
+// `hint_ns` while the phase is incomplete (it resumes when the phase
+// completes), so waiting warps leave the issue slots to working ones.
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Non-blocking test of a phase (mbarrier.test_wait): the result register
 // can be consumed later, so its latency overlaps with other work.
 __device__ __forceinline__ uint32_t mbar_probe(uint32_t bar, uint32_t parity) {
@@ -156,6 +171,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
                                           bool ignore_abort = false) {
   if (mbar_test(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w.abort, w.status, w.timeout_ns, ignore_abort);
+}
+
+// Bounded wait that sleeps between tests (see mbar_test_sleep): for roles
+// that share their SM sub-partition with warps doing arithmetic.
+static __device__ __forceinline__ bool mbar_wait_sleep_slow(uint32_t bar, uint32_t parity,
+                                                         volatile int* abort, unsigned int* status,
+                                                         unsigned long long timeout_ns, bool ignore_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_sleep(bar, parity, 20000u)) return true;
+    if ((it & 7u) == 0u) {
+      if (!ignore_abort && *abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        atomicOr(status, kDevTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                                bool ignore_abort = false) {
+  if (mbar_test(bar, parity)) return true;
+  return mbar_wait_sleep_slow(bar, parity, w.abort, w.status, w.timeout_ns, ignore_abort);
+}
+__device__ __forceinline__ bool mbar_wait_sleep_warp(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  return __all_sync(0xffffffffu, mbar_wait_sleep(bar, parity, w));
 }
 
 // Warp-uniform form for warps that go on to warp-collective instructions
@@ -264,6 +306,18 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
 }
 // Wait until every cp.async this thread issued has written shared memory.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// 4-byte asynchronous copy (src_bytes 0 writes zero), grouped with
+// cp_async_commit and waited for with cp_async_wait_group.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA, tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

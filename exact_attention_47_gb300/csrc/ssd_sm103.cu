@@ -13,14 +13,17 @@
 //     one 128 x N x chunk MMA for both heads (rows = the two heads' 64
 //     columns of x, which share B), the state staying in TMEM throughout.
 //   ssd_out_kernel: one CTA per (batch, chunk, 128-row block, up to 16 heads
-//     of one group) forms C B^T once for the group's heads in TMEM; per head
-//     its entries are weighted by 2^(g_i - g_j) under the causal mask and
-//     rounded to bf16 into TMEM (P), and
-//       y_i = (P X)_i + 2^(g_i) (C S^T)_i      (S: the chunk's initial state)
-//     with P X and C S^T as MMAs and the row factor applied on the way out.
-// Every exponent is <= 0 (a_t < 0 and the mask keeps j <= i), as the page
-// notes.  Layouts: x / y [batch, L, H, P] bf16, B / C [batch, L, G, N]
-// bf16, dt [batch, L, H] fp32, A [H] fp32, states [batch, H, P, N] fp32.
+//     of one group) forms C B^T once for the group's heads in TMEM, and per
+//     head
+//       y_i = sum_{j <= i} (C B^T)_ij 2^(g_i - g_j) x_j + 2^(g_i) (C S^T)_i
+//     (S: the chunk's initial state) with the sums as MMAs.
+// Every exponent the kernels evaluate is <= 0: the weights are only formed
+// for j <= i, where g_i <= g_j (a_t < 0), as the page notes.  Where a block
+// of keys lies wholly before a block of rows, the weight is split at a point
+// m between them, 2^(g_i - g_j) = 2^(g_i - g_m) 2^(g_m - g_j), both factors
+// <= 1: a row factor and a key factor replace one exponential per entry.
+// Layouts: x / y [batch, L, H, P] bf16, B / C [batch, L, G, N] bf16,
+// dt [batch, L, H] fp32, A [H] fp32, states [batch, H, P, N] fp32.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,10 +35,27 @@ namespace {
 
 constexpr int kP = 64;                 // head dim handled by the kernels
 constexpr int kHeadsPerOut = 16;       // heads of one group per output CTA
+constexpr int kRows = 64;              // tokens per TMA box of x and B
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
+// x <- bf16(x * w) for the 8 bf16 values of one 16-byte piece, on packed
+// bf16 pairs: w = w_hi + w_lo with both parts bf16, and
+// x w = fma(x, w_hi, x w_lo) rounded once; the error of the small term
+// x w_lo is about 2^-18 |x w|, below the final rounding.
+__device__ __forceinline__ void scale_piece_bf16(uint4* piece, float w) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+  const __nv_bfloat162 whi = __halves2bfloat162(hi, hi);
+  const __nv_bfloat162 wlo = __halves2bfloat162(lo, lo);
+  uint4 v = *piece;
+  __nv_bfloat162* vw = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) vw[e] = __hfma2(vw[e], whi, __hmul2(vw[e], wlo));
+  *piece = v;
 }
 
 // Shared-memory layouts: every tile is rows of 128 bytes (64 bf16) in the
@@ -43,15 +63,17 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // 64 columns is a sequence of such 64-column chunks.
 template <int N, int Q>
 struct StateLayout {
-  static constexpr int TB = Q < 128 ? Q : 128;   // tokens per stage (one TMA box)
+  static constexpr int TB = kRows;               // tokens per stage
   static constexpr int SPC = Q / TB;             // stages per chunk
   static constexpr int NCH = N / 64;
   static constexpr int kX = TB * 128;            // x of one head: TB rows x 64 columns
   static constexpr int kB = TB * 128;            // one 64-column chunk of B
   static constexpr int kStage = 2 * kX + NCH * kB;
   static constexpr int kStages = 3;
-  static constexpr int kOffG = kStages * kStage; // g of the current chunk: [2][Q] fp32
-  static constexpr int kOffBar = kOffG + 2 * Q * 4;
+  static constexpr int kOffW = kStages * kStage; // per-token weights [2 heads][Q] fp32
+  static constexpr int kOffGl = kOffW + 2 * Q * 4;   // g_last [2 heads]
+  static constexpr int kOffDt = kOffGl + 16;         // dt staging [2 heads][2 chunks][Q] fp32
+  static constexpr int kOffBar = kOffDt + 4 * Q * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;
 };
 
@@ -79,16 +101,20 @@ struct SsdParams {
 // ------------------------------------------------------------ state kernel
 // Warp 0: TMA producer.  Warp 1: MMA issuer (and TMEM owner).  Warps 2-5:
 // the state's 128 rows (TMEM lane = row = head pair member * 64 + p), the
-// g scans, the stored states and the scaling of x.
+// g scans (warps 2 and 3, dt fetched one chunk ahead with cp.async), the
+// stored states and the scaling of x.  Small enough for two CTAs per SM.
 template <int N, int Q>
 __global__ void __launch_bounds__(192, 1)
     ssd_state_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tb,
                      const SsdParams p) {
   using Lt = StateLayout<N, Q>;
+  constexpr int S = Lt::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   StateBars* bar = reinterpret_cast<StateBars*>(smem + Lt::kOffBar);
-  float* gs = reinterpret_cast<float*>(smem + Lt::kOffG);
+  float* ws = reinterpret_cast<float*>(smem + Lt::kOffW);
+  float* gl = reinterpret_cast<float*>(smem + Lt::kOffGl);
+  float* dtb = reinterpret_cast<float*>(smem + Lt::kOffDt);
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -103,7 +129,7 @@ __global__ void __launch_bounds__(192, 1)
   const int nstage = p.nc * Lt::SPC;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&bar->full[s]), 1);
       mbar_init(smem_addr(&bar->empty[s]), 1);
       mbar_init(smem_addr(&bar->xs[s]), 4);
@@ -117,7 +143,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   if (!has_b) {
     // The second head's rows of x stay zero (it is never loaded).
-    for (int s = 0; s < 3; ++s)
+    for (int s = 0; s < S; ++s)
       for (int i = threadIdx.x; i < Lt::kX / 16; i += blockDim.x)
         *reinterpret_cast<uint4*>(smem + s * Lt::kStage + Lt::kX + i * 16) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
@@ -137,8 +163,8 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       const uint32_t bytes = (has_b ? 2 : 1) * Lt::kX + Lt::NCH * Lt::kB;
       for (int s = 0; s < nstage; ++s) {
-        const int st = s % 3;
-        if (!mbar_wait(smem_addr(&bar->empty[st]), ((s / 3) & 1) ^ 1, wc)) break;
+        const int st = s % S;
+        if (!mbar_wait_sleep(smem_addr(&bar->empty[st]), ((s / S) & 1) ^ 1, wc)) break;
         bar->issued = s + 1;
         const int t = (s / Lt::SPC) * Q + (s % Lt::SPC) * Lt::TB;
         const uint32_t fb = smem_addr(&bar->full[st]);
@@ -154,13 +180,13 @@ __global__ void __launch_bounds__(192, 1)
     // --------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdesc = idesc_bf16_f32_ab(128, N, true, true);
     for (int c = 0; c < p.nc; ++c) {
-      if (!mbar_wait_warp(smem_addr(&bar->st_ready), c & 1, wc)) break;
+      if (!mbar_wait_sleep_warp(smem_addr(&bar->st_ready), c & 1, wc)) break;
       tc_fence_after();
       bool ok = true;
       for (int k = 0; k < Lt::SPC; ++k) {
         const int s = c * Lt::SPC + k;
-        const int st = s % 3;
-        if (!mbar_wait_warp(smem_addr(&bar->xs[st]), (s / 3) & 1, wc)) {
+        const int st = s % S;
+        if (!mbar_wait_sleep_warp(smem_addr(&bar->xs[st]), (s / S) & 1, wc)) {
           ok = false;
           break;
         }
@@ -193,6 +219,25 @@ __global__ void __launch_bounds__(192, 1)
     const int hrow = sel ? hb : ha;
     const bool vrow = sel == 0 || has_b;
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    // Scan warps: warp 2 for head a, warp 3 for head b; each lane holds E
+    // consecutive tokens of the chunk.
+    constexpr int E = Q / 32;
+    const int ssel = warp - 2;
+    const bool scan = ssel == 0 || (ssel == 1 && has_b);
+    const int h_scan = ssel ? hb : ha;
+    const float a_scan = scan ? __ldg(p.A + h_scan) : 0.f;
+    auto fetch = [&](int cc) {
+      const int tc0 = cc * Q;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int i = lane * E + e;
+        const bool in = tc0 + i < p.L;
+        const float* src = p.dt + (static_cast<size_t>(b) * p.L + (in ? tc0 + i : 0)) * p.H + h_scan;
+        cp_async4(smem_addr(dtb + (ssel * 2 + (cc & 1)) * Q + i), src, in ? 4u : 0u);
+      }
+      cp_async_commit();
+    };
+    if (scan) fetch(0);
     // Initial state: h0 or zero.
 #pragma unroll 1
     for (int c0 = 0; c0 < N; c0 += 32) {
@@ -206,6 +251,25 @@ __global__ void __launch_bounds__(192, 1)
       ATTN47_TMEM_ST32(trow + c0, v);
     }
     tmem_st_wait();
+    // x_t <- bf16(x_t * 2^(g_last - g_t)) in place for stage k of chunk c
+    // (rows past the sequence end have weight 0).
+    auto scale_stage = [&](int c, int k) {
+      const int s = c * Lt::SPC + k;
+      const int st = s % S;
+      if (!mbar_wait_sleep_warp(smem_addr(&bar->full[st]), (s / S) & 1, wc)) return false;
+      uint8_t* xs = smem + st * Lt::kStage;
+#pragma unroll 4
+      for (int q = tid; q < (has_b ? 2 : 1) * Lt::TB * 8; q += 128) {
+        const int hsel = q / (Lt::TB * 8);
+        const int row = (q >> 3) % Lt::TB;
+        scale_piece_bf16(reinterpret_cast<uint4*>(xs + hsel * Lt::kX + row * 128 + (q & 7) * 16),
+                         ws[hsel * Q + k * Lt::TB + row]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->xs[st]));
+      return true;
+    };
     // The four warps meet at two named barriers per chunk.  A warp whose
     // wait gave up skips the rest of its chunk but still reaches both
     // barriers; at the first one of the next chunk they all learn of it and
@@ -214,24 +278,26 @@ __global__ void __launch_bounds__(192, 1)
     for (int c = 0; c < p.nc; ++c) {
       const int t0 = c * Q;
       const int n_len = min(Q, p.L - t0);
-      // Every row is done with the previous chunk's g.
+      // Every row is done with the previous chunk's weights.
       if (named_barrier_or(1, 128, !ok)) {
         ok = false;
         break;
       }
-      // g of the chunk: warp 2 for head a, warp 3 for head b.  Past the end of
-      // the sequence a_t counts as 0, so g keeps the chunk's last value.
-      if (warp == 2 || (warp == 3 && has_b)) {
-        const int h = warp == 2 ? ha : hb;
-        const float a = __ldg(p.A + h);
-        constexpr int E = Q / 32;
+      if (scan) {
+        if (c + 1 < p.nc) {
+          fetch(c + 1);
+          cp_async_wait_group<1>();
+        } else {
+          cp_async_wait_group<0>();
+        }
+        // Past the end of the sequence dt reads as 0, so g keeps the
+        // chunk's last value there.
+        const float* dcur = dtb + (ssel * 2 + (c & 1)) * Q;
         float v[E];
         float run = 0.f;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const int i = lane * E + e;
-          const float d = i < n_len ? __ldg(p.dt + (static_cast<size_t>(b) * p.L + t0 + i) * p.H + h) : 0.f;
-          run = fmaf(a, d, run);
+          run = fmaf(a_scan, dcur[lane * E + e], run);
           v[e] = run;
         }
         float incl = run;
@@ -241,52 +307,33 @@ __global__ void __launch_bounds__(192, 1)
           if (lane >= o) incl += y;
         }
         const float offset = incl - run;
-        float* gw = p.g + ((static_cast<size_t>(b) * p.H + h) * p.nc + c) * Q;
+        const float g_last = __shfl_sync(0xffffffffu, incl, 31) * kLog2e;
+        float* gw = p.g + ((static_cast<size_t>(b) * p.H + h_scan) * p.nc + c) * Q;
+        float* wrow = ws + ssel * Q;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
+          const int i = lane * E + e;
           const float gv = (v[e] + offset) * kLog2e;
-          gs[(warp - 2) * Q + lane * E + e] = gv;
-          gw[lane * E + e] = gv;
+          gw[i] = gv;
+          wrow[i] = i < n_len ? ex2(g_last - gv) : 0.f;
         }
+        if (lane == 0) gl[ssel] = g_last;
       }
       named_barrier_sync(1, 128);
-      // x_t <- bf16(x_t * 2^(g_last - g_t)) in place, stage by stage (rows
-      // past the sequence end are zero and stay zero).
-      for (int k = 0; k < Lt::SPC; ++k) {
-        const int s = c * Lt::SPC + k;
-        const int st = s % 3;
-        if (!mbar_wait_warp(smem_addr(&bar->full[st]), (s / 3) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        uint8_t* xs = smem + st * Lt::kStage;
-        for (int q = tid; q < (has_b ? 2 : 1) * Lt::TB * 8; q += 128) {
-          const int hs = q / (Lt::TB * 8);
-          const int row = (q >> 3) % Lt::TB;
-          const int tt = k * Lt::TB + row;
-          const float w = tt < n_len ? ex2(gs[hs * Q + Q - 1] - gs[hs * Q + tt]) : 0.f;
-          uint4* piece = reinterpret_cast<uint4*>(xs + hs * Lt::kX + row * 128 + (q & 7) * 16);
-          uint4 v = *piece;
-          uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            vw[e] = pack_bf16x2(__uint_as_float(vw[e] << 16) * w, __uint_as_float(vw[e] & 0xffff0000u) * w);
-          *piece = v;
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&bar->xs[st]));
-      }
+      // As many stages as the ring holds are scaled before the hand-over
+      // below (they overlap with the previous chunk's MMAs); the chunk's
+      // later stages can only be loaded once its first MMAs have run.
+      constexpr int kPre = Lt::SPC < S ? Lt::SPC : S;
+      for (int k = 0; k < kPre && ok; ++k) ok = scale_stage(c, k);
       // The chunk's initial state (once the previous chunk's MMAs are
-      // complete) is stored, then decayed to the chunk's end in place.  The
-      // scaling above overlaps with those MMAs.
+      // complete) is stored, then decayed to the chunk's end in place.
       if (!ok) continue;
-      if (c > 0 && !mbar_wait_warp(smem_addr(&bar->acc_done), (c - 1) & 1, wc)) {
+      if (c > 0 && !mbar_wait_sleep_warp(smem_addr(&bar->acc_done), (c - 1) & 1, wc)) {
         ok = false;
         continue;
       }
       tc_fence_after();
-      const float decay = vrow ? ex2(gs[sel * Q + Q - 1]) : 0.f;
+      const float decay = vrow ? ex2(gl[sel]) : 0.f;
       __nv_bfloat16* si = p.s_init + ((static_cast<size_t>(b) * p.nc + c) * p.H + hrow) * kP * N + pr * N;
 #pragma unroll 1
       for (int c0 = 0; c0 < N; c0 += 32) {
@@ -310,9 +357,11 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&bar->st_ready));
+      for (int k = kPre; k < Lt::SPC && ok; ++k) ok = scale_stage(c, k);
     }
+    if (scan) cp_async_wait_group<0>();
     // Final state.
-    if (ok && mbar_wait_warp(smem_addr(&bar->acc_done), (p.nc - 1) & 1, wc)) {
+    if (ok && mbar_wait_sleep_warp(smem_addr(&bar->acc_done), (p.nc - 1) & 1, wc)) {
       tc_fence_after();
       float* hf = p.h_final + ((static_cast<size_t>(b) * p.H + hrow) * kP + pr) * N;
 #pragma unroll 1
@@ -333,9 +382,9 @@ __global__ void __launch_bounds__(192, 1)
   // Copies still in flight (a CTA that gave up early) must land first.
   if (warp == 0 && lane == 0) {
     const int issued = bar->issued;
-    for (int st = 0; st < 3 && st < issued; ++st) {
-      const int fills = (issued - 1 - st) / 3 + 1;
-      mbar_wait(smem_addr(&bar->full[st]), (fills - 1) & 1, wc, true);
+    for (int st = 0; st < S && st < issued; ++st) {
+      const int fills = (issued - 1 - st) / S + 1;
+      mbar_wait_sleep(smem_addr(&bar->full[st]), (fills - 1) & 1, wc, true);
     }
   }
   tc_fence_before();
@@ -347,29 +396,53 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ----------------------------------------------------------- output kernel
+// A CTA takes the 128 rows [R0, R0 + 128) of a chunk, R0 = 128 rb.  Keys
+// before R0 (JO of them, 0 or 128: the "off" block) lie wholly before every
+// row: their weights split at m = R0 - 1 into the row factor
+// 2^(g_i - g_m) and the key factor 2^(g_m - g_j) (applied to x_j in shared
+// memory, per head), so their C B^T entries become a head-independent bf16
+// operand formed once.  The initial state's term 2^(g_i) C S^T shares the
+// row factor once S is scaled by 2^(g_m) (<= 1), so per head
+//   y_i = Y_i + 2^(g_i - g_m) Y2_i,
+//   Y  = P X over the diagonal block,  Y2 = P_off X' + C (2^(g_m) S)^T
+// (g_m = 0 when there is no off block).  The JD keys of the row block itself
+// (the "diagonal" block) are weighted per head in 32 x 32 sub-blocks: above
+// the diagonal zero, on it the exact exponential per entry, below it split
+// at the key sub-block's last key.
 template <int N, int Q>
 struct OutLayout {
-  static constexpr int TB = Q < 128 ? Q : 128;   // rows of one TMA box
+  static constexpr int JD = Q < 128 ? Q : 128;   // keys of the diagonal block
   static constexpr int NCH = N / 64;
   static constexpr int kC = 128 * 128;           // one 64-column chunk of the C block (128 rows)
   static constexpr int kBch = Q * 128;           // one 64-column chunk of B (up to Q keys)
+  static constexpr int kPch = 128 * 128;         // one 64-key chunk of a P buffer (128 rows)
+  static constexpr int kPbuf = (JD / 64) * kPch;
   static constexpr int kX = Q * 128;             // X of one head (up to Q keys x 64)
   static constexpr int kS = 64 * 128;            // one 64-column chunk of S (64 rows)
+  // B is only read by the C B^T product; afterwards its space holds the two
+  // P buffers.
+  static constexpr int kU = NCH * kBch > 2 * kPbuf ? NCH * kBch : 2 * kPbuf;
   static constexpr int kOffC = 0;
   static constexpr int kOffB = kOffC + NCH * kC;
-  static constexpr int kOffX = kOffB + NCH * kBch;
+  static constexpr int kOffP = kOffB;
+  static constexpr int kOffX = kOffB + kU;
   static constexpr int kOffS = kOffX + 2 * kX;
   static constexpr int kOffG = kOffS + 2 * NCH * kS;
-  static constexpr int kOffBar = kOffG + 2 * Q * 4;
+  static constexpr int kOffKf = kOffG + 2 * Q * 4;   // per-warp key factors: 8 x 32 fp32
+  static constexpr int kOffBar = kOffKf + 8 * 32 * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;
-  // TMEM columns: C B^T, P (bf16 pairs), P X, C S^T.
-  static constexpr uint32_t kColCB = 0, kColP = 256, kColY = 384, kColYc = 448;
+  // TMEM columns.  C B^T lands at [128 - JO, 128 + JD): its off block at
+  // [0, 128) is turned into bf16 (P_off, at 256) first, after which those
+  // columns hold accumulator set 0 (Y, Y2); set 1 is at [320, 448).
+  static constexpr uint32_t kColCBd = 128, kColPo = 256;
+  __host__ __device__ static constexpr uint32_t col_y(int set) { return set ? 320u : 0u; }
 };
 
 struct OutBars {
   uint64_t cb_full, cb_done;
   uint64_t xf[2], xe[2];
-  uint64_t p_full, y_full, y_free, mma_drain;
+  uint64_t p_full[2], y_full[2], y_free[2];
+  uint64_t mma_drain;
   uint32_t tmem;
   int abort;
   int issued;                 // heads whose operands the producer started
@@ -377,7 +450,9 @@ struct OutBars {
 
 // Warp 0: TMA producer.  Warp 1: MMA issuer (and TMEM owner).  Warps 2-9:
 // two per TMEM lane quarter (row = lane), each taking half of the keys (P)
-// and half of the 64 output columns (epilogue).
+// and half of the 64 output columns (epilogue).  Operands, P buffers and
+// accumulators are all double-buffered by head parity, so while head k's
+// MMAs run the rows form head k+1's weights and write out head k-1.
 template <int N, int Q>
 __global__ void __launch_bounds__(320, 1)
     ssd_out_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tb,
@@ -406,8 +481,9 @@ __global__ void __launch_bounds__(320, 1)
   const int nh = min(kHeadsPerOut, hpg - hgi * kHeadsPerOut);
   const int t0 = c * Q;
   const int n_len = min(Q, p.L - t0);
-  const int J = min(Q, 128 * (rb + 1));          // keys 0 .. J-1 of the chunk
-  const int kb_count = J / Lt::TB;
+  const int JO = 128 * rb;                       // keys of the off block
+  const int J = JO + Lt::JD;                     // keys 0 .. J-1 of the chunk
+  const int kb_count = J / kRows;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_addr(&bar->cb_full), 1);
@@ -415,10 +491,10 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&bar->xf[s]), 1);
       mbar_init(smem_addr(&bar->xe[s]), 1);
+      mbar_init(smem_addr(&bar->p_full[s]), 8);
+      mbar_init(smem_addr(&bar->y_full[s]), 1);
+      mbar_init(smem_addr(&bar->y_free[s]), 8);
     }
-    mbar_init(smem_addr(&bar->p_full), 8);
-    mbar_init(smem_addr(&bar->y_full), 1);
-    mbar_init(smem_addr(&bar->y_free), 8);
     mbar_init(smem_addr(&bar->mma_drain), 1);
     bar->abort = 0;
     bar->issued = 0;
@@ -441,20 +517,20 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(fb, Lt::NCH * Lt::kC + Lt::NCH * J * 128);
 #pragma unroll
       for (int ch = 0; ch < Lt::NCH; ++ch) {
-        tma_load_4d(sbase + Lt::kOffC + ch * Lt::kC, &tc, fb, 64 * ch, grp, t0 + rb * 128, b);
+        tma_load_4d(sbase + Lt::kOffC + ch * Lt::kC, &tc, fb, 64 * ch, grp, t0 + JO, b);
         for (int kb = 0; kb < kb_count; ++kb)
-          tma_load_4d(sbase + Lt::kOffB + ch * Lt::kBch + kb * Lt::TB * 128, &tb, fb, 64 * ch, grp,
-                      t0 + kb * Lt::TB, b);
+          tma_load_4d(sbase + Lt::kOffB + ch * Lt::kBch + kb * kRows * 128, &tb, fb, 64 * ch, grp,
+                      t0 + kb * kRows, b);
       }
       for (int k = 0; k < nh; ++k) {
         const int st = k & 1;
-        if (!mbar_wait(smem_addr(&bar->xe[st]), ((k >> 1) & 1) ^ 1, wc)) break;
+        if (!mbar_wait_sleep(smem_addr(&bar->xe[st]), ((k >> 1) & 1) ^ 1, wc)) break;
         bar->issued = k + 1;
         const int h = h0 + k;
         const uint32_t xb = smem_addr(&bar->xf[st]);
         mbar_arrive_expect_tx(xb, J * 128 + Lt::NCH * Lt::kS + Q * 4);
         for (int kb = 0; kb < kb_count; ++kb)
-          tma_load_4d(sbase + Lt::kOffX + st * Lt::kX + kb * Lt::TB * 128, &tx, xb, 0, h, t0 + kb * Lt::TB, b);
+          tma_load_4d(sbase + Lt::kOffX + st * Lt::kX + kb * kRows * 128, &tx, xb, 0, h, t0 + kb * kRows, b);
         const int srow = ((b * p.nc + c) * p.H + h) * kP;
 #pragma unroll
         for (int ch = 0; ch < Lt::NCH; ++ch)
@@ -465,7 +541,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 1) {
     // --------------------------------------------------------- MMA issuer
-    bool ok = mbar_wait_warp(smem_addr(&bar->cb_full), 0, wc);
+    bool ok = mbar_wait_sleep_warp(smem_addr(&bar->cb_full), 0, wc);
     if (ok) {
       tc_fence_after();
       // C B^T: A = C (rows i, K = n), B = B (rows j, K = n), both K-major.
@@ -474,7 +550,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int kk = 0; kk < N / 16; ++kk) {
         const uint64_t ad = sdesc_sw128(sbase + Lt::kOffC + (kk >> 2) * Lt::kC + (kk & 3) * 32, 16, 1024);
         const uint64_t bd = sdesc_sw128(sbase + Lt::kOffB + (kk >> 2) * Lt::kBch + (kk & 3) * 32, 16, 1024);
-        umma_ss_warp(tmem + Lt::kColCB, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        umma_ss_warp(tmem + Lt::kColCBd - JO, ad, bd, idesc, kk > 0 ? 1u : 0u);
       }
       umma_commit_warp(smem_addr(&bar->cb_done));
     }
@@ -482,26 +558,37 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t kIdescCS = idesc_bf16_f32_ab(128, 64, false, false);
     for (int k = 0; k < nh && ok; ++k) {
       const int st = k & 1;
-      ok = mbar_wait_warp(smem_addr(&bar->xf[st]), (k >> 1) & 1, wc) &&
-           mbar_wait_warp(smem_addr(&bar->p_full), k & 1, wc) &&
-           mbar_wait_warp(smem_addr(&bar->y_free), (k & 1) ^ 1, wc);
+      const uint32_t ph = (k >> 1) & 1;
+      ok = mbar_wait_sleep_warp(smem_addr(&bar->xf[st]), ph, wc) && mbar_wait_sleep_warp(smem_addr(&bar->p_full[st]), ph, wc) &&
+           mbar_wait_sleep_warp(smem_addr(&bar->y_free[st]), ph ^ 1, wc);
       if (!ok) break;
       tc_fence_after();
-      // P X: A = P from TMEM (8 columns = 16 keys per step), B = X (keys x
-      // 64, column-contiguous: MN-major).
-      for (int kk = 0; kk < J / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(sbase + Lt::kOffX + st * Lt::kX + kk * 2048, Lt::kX, 1024);
-        umma_ts_warp(tmem + Lt::kColY, tmem + Lt::kColP + kk * 8, bd, kIdescPX, kk > 0 ? 1u : 0u);
+      const uint32_t xs = sbase + Lt::kOffX + st * Lt::kX;
+      const uint32_t pb = sbase + Lt::kOffP + st * Lt::kPbuf;
+      const uint32_t ty = tmem + Lt::col_y(st);
+      // Diagonal block: Y = P X over its JD keys (A = P, K-major in shared
+      // memory; B = X rows, column-contiguous).
+#pragma unroll
+      for (int kk = 0; kk < Lt::JD / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(pb + (kk >> 2) * Lt::kPch + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(xs + JO * 128 + kk * 2048, Lt::kX, 1024);
+        umma_ss_warp(ty, ad, bd, kIdescPX, kk > 0 ? 1u : 0u);
       }
-      // C S^T: A = C, B = S (rows p, K = n): both K-major.
+      // Off block: Y2 = P_off X' (A = P_off from TMEM, 8 columns = 16 keys
+      // per step).
+      for (int kk = 0; kk < JO / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(xs + kk * 2048, Lt::kX, 1024);
+        umma_ts_warp(ty + 64, tmem + Lt::kColPo + kk * 8, bd, kIdescPX, kk > 0 ? 1u : 0u);
+      }
+      // Y2 += C S'^T: A = C, B = S (rows p, K = n): both K-major.
 #pragma unroll
       for (int kk = 0; kk < N / 16; ++kk) {
         const uint64_t ad = sdesc_sw128(sbase + Lt::kOffC + (kk >> 2) * Lt::kC + (kk & 3) * 32, 16, 1024);
         const uint64_t bd =
             sdesc_sw128(sbase + Lt::kOffS + (st * Lt::NCH + (kk >> 2)) * Lt::kS + (kk & 3) * 32, 16, 1024);
-        umma_ss_warp(tmem + Lt::kColYc, ad, bd, kIdescCS, kk > 0 ? 1u : 0u);
+        umma_ss_warp(ty + 64, ad, bd, kIdescCS, (JO > 0 || kk > 0) ? 1u : 0u);
       }
-      umma_commit_warp(smem_addr(&bar->y_full));
+      umma_commit_warp(smem_addr(&bar->y_full[st]));
       umma_commit_warp(smem_addr(&bar->xe[st]));
     }
     umma_commit_warp(smem_addr(&bar->mma_drain));
@@ -510,91 +597,153 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------- rows
     const int wq = warp & 3;
     const int hf = (warp - 2) >> 2;            // half of the keys / of the output columns
-    const int r = wq * 32 + lane;
-    const int i_abs = rb * 128 + r;            // row's position in the chunk
+    const int tid = threadIdx.x - 64;          // 0 .. 255
+    const int r = wq * 32 + lane;              // row within the block
+    const int i_abs = JO + r;                  // row's position in the chunk
     const uint32_t trow = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float* gsm_base = reinterpret_cast<const float*>(smem + Lt::kOffG);
-    auto epilogue = [&](int k, float gi) {
-      uint32_t yv[32], cv[32];
-      ATTN47_TMEM_LD32(trow + Lt::kColY + hf * 32, yv);
-      ATTN47_TMEM_LD32(trow + Lt::kColYc + hf * 32, cv);
-      ATTN47_TMEM_LD_WAIT(yv);
-      ATTN47_TMEM_LD_WAIT(cv);
-      if (i_abs < n_len) {
-        const float w = ex2(gi);
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.y + ((static_cast<size_t>(b) * p.L + t0 + i_abs) * p.H + h0 + k) * kP + hf * 32);
+    float* kf = reinterpret_cast<float*>(smem + Lt::kOffKf) + (warp - 2) * 32;
+    auto epilogue = [&](int k, float f) {
+      const int set = k & 1;
+      const bool write = i_abs < n_len;
+      __nv_bfloat16* yrow = p.y + ((static_cast<size_t>(b) * p.L + t0 + i_abs) * p.H + h0 + k) * kP + hf * 32;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t o[4];
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t col = Lt::col_y(set) + hf * 32 + half * 16;
+        uint32_t yv[16], zv[16];
+        ATTN47_TMEM_LD16(trow + col, yv);
+        ATTN47_TMEM_LD16(trow + col + 64, zv);
+        ATTN47_TMEM_LD16_WAIT(yv);
+        ATTN47_TMEM_LD16_WAIT(zv);
+        if (write) {
+          uint32_t o[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = 8 * q + 2 * e;
-            o[e] = pack_bf16x2(fmaf(w, __uint_as_float(cv[cc]), __uint_as_float(yv[cc])),
-                               fmaf(w, __uint_as_float(cv[cc + 1]), __uint_as_float(yv[cc + 1])));
-          }
-          dst[q] = make_uint4(o[0], o[1], o[2], o[3]);
+          for (int e = 0; e < 8; ++e)
+            o[e] = pack_bf16x2(fmaf(f, __uint_as_float(zv[2 * e]), __uint_as_float(yv[2 * e])),
+                               fmaf(f, __uint_as_float(zv[2 * e + 1]), __uint_as_float(yv[2 * e + 1])));
+          uint4* dst = reinterpret_cast<uint4*>(yrow + half * 16);
+          dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->y_free));
+      if (lane == 0) mbar_arrive(smem_addr(&bar->y_free[set]));
     };
-    bool ok = mbar_wait_warp(smem_addr(&bar->cb_done), 0, wc);
+    bool ok = mbar_wait_sleep_warp(smem_addr(&bar->cb_done), 0, wc);
     tc_fence_after();
-    float g_prev = 0.f;
-    int k = 0;
-    for (; k < nh && ok; ++k) {
+    if (ok && JO > 0) {
+      // P_off = bf16(C B^T) over the off block, once for every head: this
+      // warp's 64 keys of it.
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t v[32], w[16];
+        ATTN47_TMEM_LD32(trow + hf * 64 + part * 32, v);
+        ATTN47_TMEM_LD_WAIT(v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        ATTN47_TMEM_ST16(trow + Lt::kColPo + hf * 32 + part * 16, w);
+      }
+    }
+    float f_prev = 0.f;
+    for (int k = 0; k < nh && ok; ++k) {
       const int st = k & 1;
-      if (!mbar_wait_warp(smem_addr(&bar->xf[st]), (k >> 1) & 1, wc)) {
+      if (!mbar_wait_sleep_warp(smem_addr(&bar->xf[st]), (k >> 1) & 1, wc)) {
         ok = false;
         break;
       }
+      const float* gsm = gsm_base + st * Q;
+      const float gi = gsm[min(i_abs, Q - 1)];
+      const float gm = JO > 0 ? gsm[JO - 1] : 0.f;
+      if (JO > 0) {
+        // x_j <- bf16(x_j * 2^(g_m - g_j)) over the off block's keys, and
+        // S <- bf16(S * 2^(g_m)).
+        uint8_t* xs = smem + Lt::kOffX + st * Lt::kX;
+#pragma unroll 2
+        for (int q = tid; q < JO * 8; q += 256) {
+          const int row = q >> 3;
+          scale_piece_bf16(reinterpret_cast<uint4*>(xs + row * 128 + (q & 7) * 16), ex2(gm - gsm[row]));
+        }
+        const float sf = ex2(gm);
+        uint8_t* ss = smem + Lt::kOffS + st * Lt::NCH * Lt::kS;
+#pragma unroll 2
+        for (int q = tid; q < Lt::NCH * Lt::kS / 16; q += 256) scale_piece_bf16(reinterpret_cast<uint4*>(ss + q * 16), sf);
+      }
+      // Diagonal block weights into P buffer st (bf16, K-major, 128-byte
+      // swizzle), this warp's half of the keys in 32-key sub-blocks
+      // (sub-block index sb; the rows' sub-block is wq).
+      uint8_t* prow = smem + Lt::kOffP + st * Lt::kPbuf + r * 128;
+#pragma unroll
+      for (int part = 0; part < Lt::JD / 64; ++part) {
+        const int sb = hf * (Lt::JD / 64) + part;
+        uint32_t w[16];
+        if (sb > wq) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = 0u;
+        } else {
+          uint32_t v[32];
+          ATTN47_TMEM_LD32(trow + Lt::kColCBd + sb * 32, v);
+          const float* gk = gsm + JO + sb * 32;
+          if (sb == wq) {
+            ATTN47_TMEM_LD_WAIT(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = sb * 32 + 2 * e;
+              const float p0 = j <= r ? __uint_as_float(v[2 * e]) * ex2(gi - gk[2 * e]) : 0.f;
+              const float p1 = j + 1 <= r ? __uint_as_float(v[2 * e + 1]) * ex2(gi - gk[2 * e + 1]) : 0.f;
+              w[e] = pack_bf16x2(p0, p1);
+            }
+          } else {
+            // Split at the sub-block's last key m: row factor 2^(g_i - g_m),
+            // key factors 2^(g_m - g_j) (one per lane, shared via smem).
+            const float gsub = gk[31];
+            kf[lane] = ex2(gsub - gk[lane]);
+            const float a = ex2(gi - gsub);
+            __syncwarp();
+            ATTN47_TMEM_LD_WAIT(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * a * kf[2 * e],
+                                 __uint_as_float(v[2 * e + 1]) * a * kf[2 * e + 1]);
+            __syncwarp();
+          }
+        }
+        // Keys sb*32 .. sb*32+31: 16-byte units (sb & 1) * 4 + u of 64-key
+        // chunk sb >> 1, each at its swizzled place in the row.
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (sb & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(prow + (sb >> 1) * Lt::kPch + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
+      }
+      if (k == 0 && JO > 0) tmem_st_wait();    // P_off is an operand of every head
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full[st]));
       if (k > 0) {
-        if (!mbar_wait_warp(smem_addr(&bar->y_full), (k - 1) & 1, wc)) {
+        if (!mbar_wait_sleep_warp(smem_addr(&bar->y_full[(k - 1) & 1]), ((k - 1) >> 1) & 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        epilogue(k - 1, g_prev);
+        epilogue(k - 1, f_prev);
       }
-      // P = (C B^T) o 2^(g_i - g_j) under the causal mask, this warp's half
-      // of the keys, 32 at a time (16 bf16 pairs per TMEM column group).
-      const float* gsm = gsm_base + st * Q;
-      const float gi = gsm[min(i_abs, Q - 1)];
-      const int j0 = hf * (J >> 1);
-      for (int jg = 0; jg < (J >> 1); jg += 32) {
-        uint32_t v[32];
-        ATTN47_TMEM_LD32(trow + Lt::kColCB + j0 + jg, v);
-        ATTN47_TMEM_LD_WAIT(v);
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int j = j0 + jg + 2 * e;
-          const float p0 = j <= i_abs ? __uint_as_float(v[2 * e]) * ex2(gi - gsm[j]) : 0.f;
-          const float p1 = j + 1 <= i_abs ? __uint_as_float(v[2 * e + 1]) * ex2(gi - gsm[j + 1]) : 0.f;
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        ATTN47_TMEM_ST16(trow + Lt::kColP + ((j0 + jg) >> 1), w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
-      g_prev = gi;
+      f_prev = ex2(gi - gm);
     }
-    if (ok && nh > 0 && mbar_wait_warp(smem_addr(&bar->y_full), (nh - 1) & 1, wc)) {
+    if (ok && nh > 0 && mbar_wait_sleep_warp(smem_addr(&bar->y_full[(nh - 1) & 1]), ((nh - 1) >> 1) & 1, wc)) {
       tc_fence_after();
-      epilogue(nh - 1, g_prev);
+      epilogue(nh - 1, f_prev);
     }
   }
   // Copies still in flight (a CTA that gave up early) must land first.
   if (warp == 0 && lane == 0) {
-    mbar_wait(smem_addr(&bar->cb_full), 0, wc, true);
+    mbar_wait_sleep(smem_addr(&bar->cb_full), 0, wc, true);
     const int issued = bar->issued;
     for (int st = 0; st < 2 && st < issued; ++st) {
       const int fills = (issued - 1 - st) / 2 + 1;
-      mbar_wait(smem_addr(&bar->xf[st]), (fills - 1) & 1, wc, true);
+      mbar_wait_sleep(smem_addr(&bar->xf[st]), (fills - 1) & 1, wc, true);
     }
   }
   tc_fence_before();

@@ -18,8 +18,8 @@ struct SsdLaunch {
   float* h_final;         // [batch, H, P, N]
   void* workspace;        // ssd_workspace_bytes(...)
   // TMA maps (128-byte swizzle): x as (P, H, L, batch) with box
-  // (64, 1, min(chunk, 128), 1); B the same over (N, G, L, batch); C with
-  // box (64, 1, 128, 1); the chunk states in the workspace as
+  // (64, 1, 64, 1); B the same over (N, G, L, batch); C with box
+  // (64, 1, 128, 1); the chunk states in the workspace as
   // (N, batch * nc * H * P) with box (64, 64).
   const CUtensorMap* tx;
   const CUtensorMap* tb;

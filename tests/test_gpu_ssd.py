@@ -2,10 +2,12 @@
 
 Tolerance (the pages state none).  The kernels round x * 2^(g_last - g_j),
 the decay-weighted C B^T entries and each chunk's initial state to bf16
-before their matrix products, accumulate in fp32 and round y to bf16: the
-same rounding steps as the attention forward's P, so its bounds are carried
-over relative to the output's scale: max |y - ref| <= 2e-2 * max |ref|,
-mean |y - ref| <= 2e-3 * max |ref|; the same for the final state.
+before their matrix products (for the second half of a 256-token chunk also
+x * 2^(g_m - g_j) and the state times 2^(g_m), m = 127), accumulate in fp32
+and round y to bf16: the same kind of rounding steps as the attention
+forward's P, so its bounds are carried over relative to the output's scale:
+max |y - ref| <= 2e-2 * max |ref|, mean |y - ref| <= 2e-3 * max |ref|; the
+same for the final state.
 """
 
 import numpy as np
