@@ -33,4 +33,5 @@ from ._binding import (  # noqa: F401
     ssd_chunked_fwd,
     ssd_workspace_size,
     status_string,
+    swiglu_projection,
 )

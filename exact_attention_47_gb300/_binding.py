@@ -38,6 +38,7 @@ _SIGS = {
                                 ctypes.c_float, _P, _P, _P]),
     "fused_add_rmsnorm": (_I, [_P, _P, _P, _P, _I, _I, ctypes.c_float, _P]),
     "fused_swiglu": (_I, [_P, _P, _I, _I, _P]),
+    "swiglu_projection": (_I, [_P, _P, _P, _I, _I, _I, _P]),
     "ssd_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "ssd_chunked_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                              ctypes.c_size_t, _P]),
@@ -346,6 +347,23 @@ def fused_swiglu(gate_up, out=None, stream=None):
     rows, F = gate_up.shape[0], gate_up.shape[1] // 2
     out = _output("out", out, (rows, F), torch.bfloat16, dev)
     _call("fused_swiglu", dev, _ptr(gate_up), _ptr(out), rows, F, _stream_handle(stream, dev))
+    return out
+
+
+def swiglu_projection(x, w_gate_up, out=None, stream=None):
+    """Gate/up projection with the SwiGLU activation fused in:
+    x [rows, hidden] bf16, w_gate_up [2F, hidden] bf16 (gate rows first);
+    returns silu(x W_gate^T) * (x W_up^T) [rows, F] bf16."""
+    _need_cuda("x", x, torch.bfloat16)
+    dev = x.device
+    _need_cuda("w_gate_up", w_gate_up, torch.bfloat16, dev)
+    if x.dim() != 2 or w_gate_up.dim() != 2 or w_gate_up.shape[1] != x.shape[1] or w_gate_up.shape[0] % 2:
+        raise ValueError("x must be [rows, hidden] and w_gate_up [2F, hidden]")
+    rows, hidden = x.shape
+    F = w_gate_up.shape[0] // 2
+    out = _output("out", out, (rows, F), torch.bfloat16, dev)
+    _call("swiglu_projection", dev, _ptr(x), _ptr(w_gate_up), _ptr(out), rows, hidden, F,
+          _stream_handle(stream, dev))
     return out
 
 

@@ -24,7 +24,7 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_NAME = "libattn47_sm103.so"
 LIB_PATH = os.path.join(LIB_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "fwd_sm103.cu", "bwd_sm103.cu", "decode_sm103.cu", "kv_append_sm103.cu", "fusion_sm103.cu", "ssd_sm103.cu"]
+SOURCES = ["api.cu", "fwd_sm103.cu", "bwd_sm103.cu", "decode_sm103.cu", "kv_append_sm103.cu", "fusion_sm103.cu", "gemm_sm103.cu", "ssd_sm103.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = GENCODE + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                     "-I", INCLUDE, "-I", CSRC]

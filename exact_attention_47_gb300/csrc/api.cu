@@ -15,6 +15,7 @@
 #include "decode_sm103.h"
 #include "bwd_sm103.h"
 #include "fusion_sm103.h"
+#include "gemm_sm103.h"
 #include "fwd_sm103.h"
 #include "ssd_sm103.h"
 #include "ptx.cuh"
@@ -717,6 +718,53 @@ attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void
   a.sms = dev->sms;
   a.stream = static_cast<cudaStream_t>(stream);
   return launch_result(attn47::launch_swiglu_sm103(a), "fused_swiglu");
+}
+
+attn_status_t swiglu_projection(const void* x, const void* w_gate_up, void* out, int rows, int hidden,
+                                int F, void* stream) {
+  if (rows < 0 || hidden < 1 || F < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must satisfy rows >= 0, hidden >= 1, F >= 1");
+  if (hidden % attn47::swiglu_proj_k_step() != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "hidden (%d) must be a multiple of %d", hidden, attn47::swiglu_proj_k_step());
+  if (F % attn47::swiglu_proj_tile_features() != 0)
+    return fail(ATTN_ERR_UNSUPPORTED, "F (%d) must be a multiple of %d", F, attn47::swiglu_proj_tile_features());
+  if (static_cast<long long>(rows) > 0x7fffffffLL - 128 || 2LL * F > 0x7fffffffLL)
+    return fail(ATTN_ERR_UNSUPPORTED, "problem too large for one launch");
+  if (rows == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!x || !w_gate_up || !out) return fail(ATTN_ERR_INVALID_ARG, "x, w_gate_up and out must be non-null");
+  if (!aligned16(x) || !aligned16(w_gate_up) || !aligned16(out))
+    return fail(ATTN_ERR_INVALID_ARG, "x, w_gate_up and out must be 16-byte aligned");
+  const size_t xb = static_cast<size_t>(rows) * hidden * 2;
+  const size_t wb = static_cast<size_t>(2) * F * hidden * 2;
+  const size_t ob = static_cast<size_t>(rows) * F * 2;
+  if (overlap(out, ob, x, xb) || overlap(out, ob, w_gate_up, wb))
+    return fail(ATTN_ERR_INVALID_ARG, "out must not overlap x or w_gate_up");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  if ((st = check_bufs(*dev, {{x, xb, "x"}, {w_gate_up, wb, "w_gate_up"}, {out, ob, "out"}})) != ATTN_OK)
+    return st;
+  CUtensorMap tx, tw;
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint64_t xdims[2] = {static_cast<cuuint64_t>(hidden), static_cast<cuuint64_t>(rows)};
+  if ((st = encode_bf16(&tx, x, 2, xdims, box)) != ATTN_OK) return st;
+  const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(hidden), static_cast<cuuint64_t>(2) * F};
+  if ((st = encode_bf16(&tw, w_gate_up, 2, wdims, box)) != ATTN_OK) return st;
+  attn47::SwigluProjLaunch a;
+  a.tx = &tx;
+  a.tw = &tw;
+  a.out = out;
+  a.rows = rows;
+  a.F = F;
+  a.hidden = hidden;
+  a.sms = dev->sms;
+  a.status = dev->status;
+  a.timeout_ns = g_timeout_ns;
+  a.stream = static_cast<cudaStream_t>(stream);
+  return launch_result(attn47::launch_swiglu_proj_sm103(a), "swiglu_projection");
 }
 
 size_t ssd_workspace_size(int batch, int L, int H, int N, int chunk) {

@@ -44,6 +44,8 @@
  *  fused_add_rmsnorm  residual add followed by RMSNorm, one pass
  *  fused_swiglu       SwiGLU activation silu(gate) * up of the merged
  *                     gate/up projection output, one pass
+ *  swiglu_projection  the gate/up projection GEMM with SiLU * up in its
+ *                     epilogue: only the [rows, F] product reaches HBM
  *
  * and the Mamba-2 SSD forward ("Accelerating Mamba-2 with high-performance
  * forward kernels in NVIDIA CUDA Tile"):
@@ -317,6 +319,32 @@ attn_status_t fused_add_rmsnorm(const void* x, void* residual, const void* weigh
  *  rows == 0 is an empty problem.  One kernel; deterministic.
  */
 attn_status_t fused_swiglu(const void* gate_up, void* out, int rows, int F, void* stream);
+
+/*
+ * swiglu_projection — the SwiGLU block's gate/up projection with the
+ * activation fused into the matrix product.
+ *
+ * "Fast attention kernels and operator fusion accelerate AI models",
+ * section "Operator fusion": run naively, the SwiGLU block's projection
+ * matmul writes its [rows, 2F] output to HBM and a SiLU and a product kernel
+ * read it back; fused, the projection's accumulators are activated and
+ * multiplied where they are produced and only the product is written:
+ *   out[r, f] = bf16(silu(g) * u),  silu(g) = g / (1 + exp(-g)),
+ *   g = sum_k x[r, k] W[f, k],  u = sum_k x[r, k] W[F + f, k]
+ * (fp32 accumulation on the tensor cores).  The down projection that
+ * follows is a plain GEMM and not part of this call.
+ *
+ *  x          [rows, hidden] bf16 activations
+ *  w_gate_up  [2F, hidden] bf16: the gate weight's F rows, then the up
+ *             weight's F rows (a merged gate/up weight, rows = output
+ *             features, as a linear layer stores it)
+ *  out        [rows, F] bf16 (written; must not overlap the inputs)
+ *  hidden must be a multiple of 64 and F of 128; all pointers 16-byte
+ *  aligned.  rows == 0 is an empty problem.  One persistent kernel (one
+ *  CTA per SM); deterministic.
+ */
+attn_status_t swiglu_projection(const void* x, const void* w_gate_up, void* out, int rows, int hidden,
+                                int F, void* stream);
 
 /*
  * ssd_workspace_size — bytes of device workspace ssd_chunked_fwd needs: the

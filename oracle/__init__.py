@@ -36,7 +36,7 @@ from .definitions import (  # noqa: F401
     softmax_probs,
     split_partials,
 )
-from .fusions import add_rmsnorm, round_bf16, swiglu  # noqa: F401
+from .fusions import add_rmsnorm, round_bf16, swiglu, swiglu_projection  # noqa: F401
 from .ssd import (  # noqa: F401
     ssd_chunk_cumsum,
     ssd_chunk_output,

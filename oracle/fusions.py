@@ -10,7 +10,9 @@ definitions of what the fused kernels compute.
 
 Layouts (the page fixes none): rows of a [rows, hidden] activation matrix;
 the SwiGLU input is the merged gate/up projection output [rows, 2F] with
-the gate in columns 0..F-1 and the up projection in columns F..2F-1.
+the gate in columns 0..F-1 and the up projection in columns F..2F-1; the
+merged gate/up weight is [2F, hidden] (rows = output features, gate rows
+first), as a linear layer stores it.
 """
 
 import numpy as np
@@ -53,4 +55,18 @@ def swiglu(gate_up):
     gate_up = np.asarray(gate_up, dtype=np.float64)
     F = gate_up.shape[-1] // 2
     g, u = gate_up[..., :F], gate_up[..., F:]
+    return g / (1.0 + np.exp(-g)) * u
+
+
+def swiglu_projection(x, w_gate_up):
+    """The SwiGLU block's gate/up projection followed by its activation, the
+    steps the page fuses into one kernel ("Operator fusion"):
+        g = x W_gate^T,  u = x W_up^T,  out = silu(g) * u,
+    x [rows, hidden], w_gate_up [2F, hidden] with W_gate = rows 0..F-1 and
+    W_up = rows F..2F-1.  Returns fp64 [rows, F]."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_gate_up, dtype=np.float64)
+    F = w.shape[0] // 2
+    g = x @ w[:F].T
+    u = x @ w[F:].T
     return g / (1.0 + np.exp(-g)) * u

@@ -119,6 +119,16 @@ def test_fusion_host_validation(lib):
     assert lib.fused_swiglu(FAKE, FAKE, 0, 16, None) == OK
 
 
+def test_swiglu_projection_host_validation(lib):
+    out = ctypes.c_void_p(0x400000)
+    assert lib.swiglu_projection(FAKE, ctypes.c_void_p(0x200000), out, 4, 96, 128, None) == UNSUPPORTED  # hidden
+    assert lib.swiglu_projection(FAKE, ctypes.c_void_p(0x200000), out, 4, 64, 96, None) == UNSUPPORTED   # F
+    assert lib.swiglu_projection(FAKE, ctypes.c_void_p(0x200000), FAKE, 4, 64, 128, None) == INVALID     # out is x
+    assert lib.swiglu_projection(FAKE, ctypes.c_void_p(0x200008), out, 4, 64, 128, None) == INVALID      # misaligned
+    assert lib.swiglu_projection(FAKE, None, out, 4, 64, 128, None) == INVALID
+    assert lib.swiglu_projection(FAKE, FAKE, FAKE, 0, 64, 128, None) == OK
+
+
 def _ssd(lib, batch=2, L=100, H=8, G=1, P=64, N=128, chunk=64, ws_bytes=None):
     need = lib.ssd_workspace_size(batch, L, H, N, chunk)
     return lib.ssd_chunked_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, batch, L, H, G, P, N,

@@ -1,5 +1,5 @@
 """Pins of the fp64 oracle's operator fusions (``oracle.add_rmsnorm``,
-``oracle.swiglu``, ``oracle.round_bf16``).
+``oracle.swiglu``, ``oracle.swiglu_projection``, ``oracle.round_bf16``).
 
 Each pin checks the oracle against something other than its own code:
 torch's own bf16 conversion and bf16 addition, ``torch.nn.functional.rms_norm``
@@ -99,6 +99,34 @@ def pin_swiglu_closed_forms(fn):
 SWIGLU_PINS = [(pin_swiglu_vs_torch, 1e-12), (pin_swiglu_closed_forms, 1e-12)]
 
 
+def pin_projection_vs_torch(fn):
+    """torch's fp64 matmuls of the two weight halves and its silu."""
+    x, w = workloads.swiglu_projection_inputs(29, 64, 48, seed=16)
+    xt, wt = torch.tensor(_np(x)), torch.tensor(_np(w))
+    ref = torch.nn.functional.silu(xt @ wt[:48].T) * (xt @ wt[48:].T)
+    return float(np.abs(fn(_np(x), _np(w)) - ref.numpy()).max())
+
+
+def pin_projection_identity_weights(fn):
+    """W_gate = 2 I and W_up = I (hidden = F) give silu(2 x) * x elementwise."""
+    x = np.linspace(-4.0, 4.0, 40).reshape(5, 8)
+    w = np.concatenate([2.0 * np.eye(8), np.eye(8)], axis=0)
+    return float(np.abs(fn(x, w) - 2.0 * x / (1.0 + np.exp(-2.0 * x)) * x).max())
+
+
+def pin_projection_single_feature(fn):
+    """One feature with gate weight row a and up weight row b: the gate and
+    up inputs are the dot products x.a and x.b, worked by hand."""
+    x = np.array([[1.0, 2.0, -1.0]])
+    w = np.array([[0.5, 0.0, 1.0],      # g = 0.5 - 1 = -0.5
+                  [1.0, 1.0, 1.0]])     # u = 1 + 2 - 1 = 2
+    return float(abs(fn(x, w)[0, 0] - (-0.5 / (1.0 + np.exp(0.5)) * 2.0)))
+
+
+PROJ_PINS = [(pin_projection_vs_torch, 1e-12), (pin_projection_identity_weights, 1e-12),
+             (pin_projection_single_feature, 1e-15)]
+
+
 @pytest.mark.parametrize("pin,tol", RMS_PINS, ids=lambda x: getattr(x, "__name__", str(x)))
 def test_add_rmsnorm_oracle_passes_pin(pin, tol):
     assert pin(oracle.add_rmsnorm) <= tol
@@ -107,6 +135,11 @@ def test_add_rmsnorm_oracle_passes_pin(pin, tol):
 @pytest.mark.parametrize("pin,tol", SWIGLU_PINS, ids=lambda x: getattr(x, "__name__", str(x)))
 def test_swiglu_oracle_passes_pin(pin, tol):
     assert pin(oracle.swiglu) <= tol
+
+
+@pytest.mark.parametrize("pin,tol", PROJ_PINS, ids=lambda x: getattr(x, "__name__", str(x)))
+def test_swiglu_projection_oracle_passes_pin(pin, tol):
+    assert pin(oracle.swiglu_projection) <= tol
 
 
 # ---------------------------------------------------------------- mutants
@@ -134,6 +167,23 @@ def _swiglu_mutant(kind):
     return fn
 
 
+def _projection_mutant(kind):
+    def fn(x, w_gate_up):
+        x = np.asarray(x, np.float64)
+        w = np.asarray(w_gate_up, np.float64)
+        F = w.shape[0] // 2
+        wg, wu = (w[0::2], w[1::2]) if kind == "interleaved_halves" else (w[:F], w[F:])
+        if kind == "gate_up_swapped":
+            wg, wu = wu, wg
+        g, u = x @ wg.T, x @ wu.T
+        if kind == "no_activation":
+            return g * u
+        if kind == "exp_sign":
+            return g / (1.0 + np.exp(g)) * u
+        return g / (1.0 + np.exp(-g)) * u
+    return fn
+
+
 @pytest.mark.parametrize("kind", ["unrounded_residual", "sum_not_mean", "eps_outside_sqrt", "no_weight"])
 def test_add_rmsnorm_mutant_is_caught(kind):
     assert any(not (pin(_rms_mutant(kind)) <= tol) for pin, tol in RMS_PINS), kind
@@ -144,8 +194,15 @@ def test_swiglu_mutant_is_caught(kind):
     assert any(not (pin(_swiglu_mutant(kind)) <= tol) for pin, tol in SWIGLU_PINS), kind
 
 
+@pytest.mark.parametrize("kind", ["gate_up_swapped", "interleaved_halves", "no_activation", "exp_sign"])
+def test_swiglu_projection_mutant_is_caught(kind):
+    assert any(not (pin(_projection_mutant(kind)) <= tol) for pin, tol in PROJ_PINS), kind
+
+
 def test_mutant_templates_reproduce_oracle():
     for pin, tol in RMS_PINS:
         assert pin(_rms_mutant("none")) <= tol, pin.__name__
     for pin, tol in SWIGLU_PINS:
         assert pin(_swiglu_mutant("none")) <= tol, pin.__name__
+    for pin, tol in PROJ_PINS:
+        assert pin(_projection_mutant("none")) <= tol, pin.__name__

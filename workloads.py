@@ -184,6 +184,8 @@ FUSION_CONFIGS = {
     # workload: hidden size 1536, MLP intermediate size 8960.
     "qwen_add_rmsnorm": dict(rows=16384, hidden=1536, seed=6),
     "qwen_swiglu": dict(rows=16384, F=8960, seed=7),
+    # The same layer's gate/up projection with the activation fused in.
+    "qwen_swiglu_projection": dict(rows=16384, hidden=1536, F=8960, seed=9),
 }
 
 
@@ -204,6 +206,18 @@ def swiglu_inputs(rows, F, seed):
     g = _randn(gen, (rows, F), 2.0)
     u = _randn(gen, (rows, F))
     return torch.cat([g, u], dim=1).to(torch.bfloat16)
+
+
+def swiglu_projection_inputs(rows, hidden, F, seed):
+    """Activations x [rows, hidden] ~ N(0, 1) and a merged gate/up weight
+    [2F, hidden] (gate rows first), bf16 (CPU).  Gate weights have std
+    2 / sqrt(hidden), so the projected gate is about N(0, 2^2) and SiLU sees
+    both its linear and its vanishing side; up weights 1 / sqrt(hidden)."""
+    gen = torch.Generator().manual_seed(int(seed))
+    x = _randn(gen, (rows, hidden)).to(torch.bfloat16)
+    wg = _randn(gen, (F, hidden), 2.0 / hidden ** 0.5)
+    wu = _randn(gen, (F, hidden), 1.0 / hidden ** 0.5)
+    return x, torch.cat([wg, wu], dim=0).to(torch.bfloat16)
 
 
 SSD_CONFIGS = {
