@@ -515,7 +515,13 @@ def ssd_measurement(attn, device, steps, peak_tflops, peak_gbs):
             "kernels": "chunk state (cumsum + fwd_pass_state) + chunk output", "gpu_launches_per_call": 2}
 
 
-def fusion_measurement(attn, device, steps, peak_gbs):
+def swiglu_projection_flops(rows, hidden, F):
+    """FLOPs of the gate/up projection: a [rows, hidden] x [hidden, 2F]
+    product (the activation's few operations per output are not counted)."""
+    return 2.0 * rows * 2 * F * hidden
+
+
+def fusion_measurement(attn, device, steps, peak_gbs, peak_tflops):
     """fused_add_rmsnorm and fused_swiglu on one Qwen2.5-1.5B-sized layer over
     the 16384 prefill tokens (hidden 1536, intermediate 8960), CUDA events over
     `steps` calls after 3 warm-ups.  Algorithmic bytes: every input read once,
@@ -558,6 +564,22 @@ def fusion_measurement(attn, device, steps, peak_gbs):
         gbs = b / (ms / 1e3) / 1e9
         res[name] = {"shape": shape, "ms": ms, "bytes": b, "GB/s": gbs, "frac": gbs / peak_gbs,
                      "bound": "hbm"}
+    # The gate/up projection with the activation in its epilogue, beside the
+    # unfused pair it replaces (a library GEMM writing [rows, 2F], then the
+    # activation kernel): the library GEMM is a comparison point only.
+    p = workloads.FUSION_CONFIGS["qwen_swiglu_projection"]
+    x, w = workloads.swiglu_projection_inputs(p["rows"], p["hidden"], p["F"], p["seed"])
+    x, w = x.to(device), w.to(device)
+    out = torch.empty((p["rows"], p["F"]), dtype=torch.bfloat16, device=device)
+    ms_proj = timed(lambda i: attn.swiglu_projection(x, w, out=out), steps)
+    gu = torch.empty((p["rows"], 2 * p["F"]), dtype=torch.bfloat16, device=device)
+    ms_unfused = timed(lambda i: (torch.matmul(x, w.T, out=gu), attn.fused_swiglu(gu, out=out)), steps)
+    del x, w, out, gu
+    pf = swiglu_projection_flops(p["rows"], p["hidden"], p["F"])
+    tf = pf / (ms_proj / 1e3) / 1e12
+    res["swiglu_projection"] = {"shape": "rows 16384 hidden 1536 F 8960", "ms": ms_proj, "flops": pf,
+                                "TFLOP/s": tf, "frac": tf / peak_tflops, "bound": "tensor",
+                                "unfused_library_gemm_plus_activation_ms": ms_unfused}
     return res
 
 
@@ -666,7 +688,7 @@ def run_gpu(args, rank, world, local_rank):
     fwd_configs = fwd_config_table(attn, device, side, pk_all["bf16_tflops"])
     backward = bwd_measurement(attn, device, side, pk_all["bf16_tflops"])
     paged_prefill = paged_prefill_measurement(attn, device, side, pk_all["bf16_tflops"])
-    fusions = fusion_measurement(attn, device, side, pk_all["hbm_gbs"])
+    fusions = fusion_measurement(attn, device, side, pk_all["hbm_gbs"], pk_all["bf16_tflops"])
     ssd = ssd_measurement(attn, device, side, pk_all["bf16_tflops"], pk_all["hbm_gbs"])
 
     # ---- max over ranks

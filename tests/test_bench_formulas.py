@@ -75,3 +75,9 @@ def test_ssd_bytes_lists_every_tensor():
     reads = sum(t.numel() * t.element_size() for t in d.values())      # x, dt, A, B, C
     writes = batch * L * H * P * 2 + batch * H * P * N * 4             # y (bf16), final state (fp32)
     assert bench.ssd_bytes(batch, L, H, G, P, N) == reads + writes
+
+
+def test_swiglu_projection_flops_is_the_gemm():
+    # [rows, hidden] x [hidden, 2F]: one multiply-add per (row, output column, k).
+    rows, hidden, F = 5, 64, 128
+    assert bench.swiglu_projection_flops(rows, hidden, F) == 2 * rows * (2 * F) * hidden
