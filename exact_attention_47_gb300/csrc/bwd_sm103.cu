@@ -35,10 +35,17 @@ constexpr int kThreads = 320;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr int kComputeWarps = 8;
-// TMEM column of the packed bf16 operand for K step kk (16 keys / queries):
-// keys 64h + 2c, 64h + 2c + 1 live in column 64h + c.
-__device__ __forceinline__ uint32_t packed_col(int kk) {
-  return static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+// TMEM columns of the two halves of a step's 128 x 128 score tile (64
+// columns each): S_h at 128 h, dP_h at 128 h + 64; the accumulators sit at
+// 256 and up.
+__device__ __forceinline__ uint32_t col_s(int h) { return static_cast<uint32_t>(h * 128); }
+__device__ __forceinline__ uint32_t col_dp(int h) { return static_cast<uint32_t>(h * 128 + 64); }
+// Column, relative to a half, of the packed bf16 operand for K step kk (16
+// of its 64 keys / queries): each compute warp packs its 32 values 2 per
+// column over the first 16 of its own 32 columns, so values 2c, 2c + 1 of
+// warp part w live in column 32 w + c.
+__device__ __forceinline__ uint32_t half_col(int kk) {
+  return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8);
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -64,8 +71,8 @@ struct BwdLayout {
 struct BwdBarriers {
   uint64_t once_full;                 // the tiles loaded once per CTA
   uint64_t st_full[2], st_empty[2];   // per-stage tiles (and vectors)
-  uint64_t s_full;                    // S and dP of a step are in TMEM
-  uint64_t p_full;                    // the compute warps wrote P / dS
+  uint64_t s_full[2];                 // S and dP of a half are in TMEM
+  uint64_t p_full[2];                 // the compute warps wrote a half's P / dS
   uint64_t done;                      // last accumulating MMA completed
   uint64_t mma_final;
   uint32_t tmem_base;
@@ -104,22 +111,21 @@ __global__ void __launch_bounds__(256) attn_bwd_rowdot_kernel(const BwdParams p)
   }
 }
 
-// The two 32-column chunks of this warp's 64 columns (64 h ..) of two TMEM
-// rows (a, b) -> BODY on the fp32 values of each chunk; BODY's 32 packed bf16
-// words are then stored over columns [64 h, 64 h + 32) of a, which this warp
-// has read already.
-#define ATTN47_BWD_ROW_LOOP(TA, TB, H, BODY)                                                   \
-  uint32_t pk[32];                                                                             \
-  _Pragma("unroll") for (int sub = 0; sub < 2; ++sub) {                                        \
-    const int chunk = (H) * 2 + sub;                                                           \
-    uint32_t ra[32], rb[32];                                                                   \
-    ATTN47_TMEM_LD32((TA) + chunk * 32, ra);                                                   \
-    ATTN47_TMEM_LD32((TB) + chunk * 32, rb);                                                   \
-    ATTN47_TMEM_LD_WAIT(ra);                                                                   \
-    ATTN47_TMEM_LD_WAIT(rb);                                                                   \
-    _Pragma("unroll") for (int c2 = 0; c2 < 16; ++c2) { BODY }                                 \
-  }                                                                                            \
-  ATTN47_TMEM_ST32((TA) + (H) * 64, pk);
+__device__ __forceinline__ void init_barriers(BwdBarriers* bar, int tid) {
+  if (tid == 0) {
+    mbar_init(smem_addr(&bar->once_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&bar->st_full[s]), 1);
+      mbar_init(smem_addr(&bar->st_empty[s]), 1);
+      mbar_init(smem_addr(&bar->s_full[s]), 1);
+      mbar_init(smem_addr(&bar->p_full[s]), kComputeWarps);
+    }
+    mbar_init(smem_addr(&bar->done), 1);
+    mbar_init(smem_addr(&bar->mma_final), 1);
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+}
 
 // ------------------------------------------------------------------- dQ
 template <int D, bool CAUSAL>
@@ -129,8 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
   const uint32_t sQ = smem_addr(smem + L::kOffA);
   const uint32_t sDO = smem_addr(smem + L::kOffB);
@@ -145,19 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kv_total = nq;
   const int n_kv = CAUSAL ? min(qt + 1, kv_total) : kv_total;
 
-  if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar->once_full), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(smem_addr(&bar->st_full[s]), 1);
-      mbar_init(smem_addr(&bar->st_empty[s]), 1);
-    }
-    mbar_init(smem_addr(&bar->s_full), 1);
-    mbar_init(smem_addr(&bar->p_full), kComputeWarps);
-    mbar_init(smem_addr(&bar->done), 1);
-    mbar_init(smem_addr(&bar->mma_final), 1);
-    bar->abort = 0;
-    fence_mbar_init();
-  }
+  init_barriers(bar, threadIdx.x);
   if (warp == kWarpMma) {
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -167,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  constexpr uint32_t kColDQ = 256;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
@@ -203,44 +196,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // --------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false);
+    // Per K/V tile j and key half h (keys 64 h .. 64 h + 63 of the tile):
+    //   S_h = Q K_h^T, dP_h = dO V_h^T            (sdp)
+    //   dQ += dS_h K_h, dS_h bf16 over S_h        (acc)
+    // issued as sdp(0, j) sdp(1, j) | acc(0, j) sdp(0, j+1) | acc(1, j)
+    // sdp(1, j+1) | ..., so the tensor core works on one half while the
+    // compute warps turn the other into dS.
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, 64, false);
     constexpr uint32_t kIdescDQ = idesc_bf16_f32(kTile, D, true);
-    auto ss_group = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+    auto sdp = [&](int h, uint32_t kb) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ad = sdesc_sw128(a_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(b_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
-        umma_ss_warp(tmem + d_col, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        const uint32_t o = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+        umma_ss_warp(tmem + col_s(h), sdesc_sw128(sQ + o, 16, 1024), sdesc_sw128(kb + o + h * 8192, 16, 1024),
+                     kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+        umma_ss_warp(tmem + col_dp(h), sdesc_sw128(sDO + o, 16, 1024),
+                     sdesc_sw128(kb + L::kTileBytes + o + h * 8192, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto acc = [&](int h, uint32_t kb, bool first) {
+      // B = K_h as K x N with N = d contiguous.
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bd = sdesc_sw128(kb + h * 8192 + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDQ, tmem + col_s(h) + half_col(kk), bd, kIdescDQ, (first && kk == 0) ? 0u : 1u);
       }
     };
     bool ok = mbar_wait_warp(smem_addr(&bar->once_full), 0, wc) &&
               mbar_wait_warp(smem_addr(&bar->st_full[0]), 0, wc);
     if (ok) {
       tc_fence_after();
-      ss_group(kColS, sQ, sSt);                                  // S = Q K_0^T
-      ss_group(kColDP, sDO, sSt + L::kTileBytes);                // dP = dO V_0^T
-      umma_commit_warp(smem_addr(&bar->s_full));
+      sdp(0, sSt);
+      umma_commit_warp(smem_addr(&bar->s_full[0]));
+      sdp(1, sSt);
+      umma_commit_warp(smem_addr(&bar->s_full[1]));
     }
     for (int j = 0; j < n_kv && ok; ++j) {
       const int st = j % L::kStages;
-      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full), j & 1, wc))) break;
-      tc_fence_after();
-      // dQ += dS K_j: A = dS (bf16 over S), B = K_j as K x N with N = d contiguous.
       const uint32_t kb = sSt + st * L::kStageBytes;
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(kb + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDQ, tmem + kColS + packed_col(kk), bd, kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      umma_commit_warp(smem_addr(&bar->st_empty[st]));
-      if (j + 1 < n_kv) {
-        const int st1 = (j + 1) % L::kStages;
-        if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[st1]), ((j + 1) / L::kStages) & 1, wc))) break;
+      const bool next = j + 1 < n_kv;
+      const uint32_t kb1 = sSt + ((j + 1) % L::kStages) * L::kStageBytes;
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full[0]), j & 1, wc))) break;
+      tc_fence_after();
+      acc(0, kb, j == 0);
+      if (next) {
+        if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[(j + 1) % L::kStages]), ((j + 1) / L::kStages) & 1, wc)))
+          break;
         tc_fence_after();
-        const uint32_t b1 = sSt + st1 * L::kStageBytes;
-        ss_group(kColS, sQ, b1);
-        ss_group(kColDP, sDO, b1 + L::kTileBytes);
-        umma_commit_warp(smem_addr(&bar->s_full));
+        sdp(0, kb1);
+        umma_commit_warp(smem_addr(&bar->s_full[0]));
+      }
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full[1]), j & 1, wc))) break;
+      tc_fence_after();
+      acc(1, kb, false);
+      umma_commit_warp(smem_addr(&bar->st_empty[st]));
+      if (next) {
+        sdp(1, kb1);
+        umma_commit_warp(smem_addr(&bar->s_full[1]));
       }
     }
     umma_commit_warp(smem_addr(&bar->done));
@@ -248,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
   } else {
     // -------------------------------------------------------- compute warps
-    const int quarter = warp & 3, h = warp >> 2;   // lane quarter, column half
+    const int quarter = warp & 3, w2 = warp >> 2;  // lane quarter, 32-column part of each half
     const int row = quarter * 32 + lane;          // TMEM lane = query row within the tile
     const int qrow = qt * kTile + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -257,31 +273,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float dr = p.ws_d[vrow];
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(smem_addr(&bar->s_full), j & 1, wc)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    for (int j = 0; j < n_kv && ok; ++j) {
       const int kbase = j * kTile;
-      const bool need_mask = (CAUSAL && j == qt) || (kbase + kTile > p.N);
-      // dS = P * (dP - D), P = 2^(s * scale * log2 e - lse * log2 e); masked keys get P = 0.
-      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, h, {
-        const int c = c2 * 2;
-        float dsv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int key = kbase + chunk * 32 + c + e;
-          const bool masked = need_mask && ((CAUSAL && key > qrow) || key >= p.N);
-          const float pv = masked ? 0.f : ex2(__uint_as_float(ra[c + e]) * sl2 - lse2);
-          dsv[e] = pv * (__uint_as_float(rb[c + e]) - dr);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait_warp(smem_addr(&bar->s_full[h]), j & 1, wc)) {
+          ok = false;
+          break;
         }
-        pk[sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
-      })
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+        tc_fence_after();
+        // dS = P * (dP - D), P = 2^(s * scale * log2 e - lse * log2 e);
+        // masked keys get P = 0.  32 keys of half h per warp.
+        const uint32_t cs = col_s(h) + w2 * 32, cd = col_dp(h) + w2 * 32;
+        uint32_t ra[32], rb[32], pk[16];
+        ATTN47_TMEM_LD32(tl + cs, ra);
+        ATTN47_TMEM_LD32(tl + cd, rb);
+        ATTN47_TMEM_LD_WAIT(ra);
+        ATTN47_TMEM_LD_WAIT(rb);
+        // Keys k0 + c are allowed for c < hi (causal: key <= qrow; all:
+        // key < N); the exponential is formed for every key and the masked
+        // ones are then selected away, which keeps the loop free of branches.
+        const int k0 = kbase + h * 64 + w2 * 32;
+        const int hi = CAUSAL ? min(qrow - k0 + 1, p.N - k0) : p.N - k0;
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          float dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * c2 + e;
+            const float ev = ex2(__uint_as_float(ra[c]) * sl2 - lse2);
+            const float pv = c < hi ? ev : 0.f;
+            dsv[e] = pv * (__uint_as_float(rb[c]) - dr);
+          }
+          pk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        ATTN47_TMEM_ST16(tl + cs, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bar->p_full[h]));
+      }
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(smem_addr(&bar->done), 0, wc)) {
@@ -289,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool in_range = qrow < p.N;
       __nv_bfloat16* dst = p.dq + (static_cast<size_t>(bh) * p.N + qrow) * D;
 #pragma unroll 1
-      for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+      for (int c0 = w2 * (D / 2); c0 < (w2 + 1) * (D / 2); c0 += 32) {
         uint32_t o[32];
         ATTN47_TMEM_LD32(tl + kColDQ + c0, o);
         ATTN47_TMEM_LD_WAIT(o);
@@ -321,8 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(smem + L::kOffBar);
   const uint32_t sK = smem_addr(smem + L::kOffA);
   const uint32_t sV = smem_addr(smem + L::kOffB);
@@ -344,19 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qt = qt0 + t % per_head;
   };
 
-  if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar->once_full), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(smem_addr(&bar->st_full[s]), 1);
-      mbar_init(smem_addr(&bar->st_empty[s]), 1);
-    }
-    mbar_init(smem_addr(&bar->s_full), 1);
-    mbar_init(smem_addr(&bar->p_full), kComputeWarps);
-    mbar_init(smem_addr(&bar->done), 1);
-    mbar_init(smem_addr(&bar->mma_final), 1);
-    bar->abort = 0;
-    fence_mbar_init();
-  }
+  init_barriers(bar, threadIdx.x);
   if (warp == kWarpMma) {
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
@@ -366,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
@@ -407,92 +425,142 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // --------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false);
+    // Per step t (a query tile of one query head) and query half h
+    // (queries 64 h .. 64 h + 63 of the tile):
+    //   S_h^T = K Q_h^T, dP_h^T = V dO_h^T                (sdp)
+    //   dV += P_h^T dO_h, dK += dS_h^T Q_h                 (acc)
+    // issued as sdp(0, t) sdp(1, t) | acc(0, t) sdp(0, t+1) | acc(1, t)
+    // sdp(1, t+1) | ..., so the tensor core works on one half while the
+    // compute warps turn the other into P^T and dS^T.
+    constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, 64, false);
     constexpr uint32_t kIdescAcc = idesc_bf16_f32(kTile, D, true);
-    auto ss_group = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+    auto sdp = [&](int h, uint32_t qb) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t ad = sdesc_sw128(a_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = sdesc_sw128(b_base + (kk >> 2) * L::kChunkBytes + (kk & 3) * 32, 16, 1024);
-        umma_ss_warp(tmem + d_col, ad, bd, kIdescS, kk > 0 ? 1u : 0u);
+        const uint32_t o = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+        umma_ss_warp(tmem + col_s(h), sdesc_sw128(sK + o, 16, 1024), sdesc_sw128(qb + o + h * 8192, 16, 1024),
+                     kIdescS, kk > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t o = (kk >> 2) * L::kChunkBytes + (kk & 3) * 32;
+        umma_ss_warp(tmem + col_dp(h), sdesc_sw128(sV + o, 16, 1024),
+                     sdesc_sw128(qb + L::kTileBytes + o + h * 8192, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
       }
     };
-    bool ok = mbar_wait_warp(smem_addr(&bar->once_full), 0, wc);
+    auto acc = [&](int h, uint32_t qb, bool first) {
+      // B = dO_h / Q_h as K x N with N = d contiguous.
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bdo = sdesc_sw128(qb + L::kTileBytes + h * 8192 + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDV, tmem + col_s(h) + half_col(kk), bdo, kIdescAcc, (first && kk == 0) ? 0u : 1u);
+      }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t bq = sdesc_sw128(qb + h * 8192 + kk * 2048, L::kChunkBytes, 1024);
+        umma_ts_warp(tmem + kColDK, tmem + col_dp(h) + half_col(kk), bq, kIdescAcc, (first && kk == 0) ? 0u : 1u);
+      }
+    };
+    bool ok = mbar_wait_warp(smem_addr(&bar->once_full), 0, wc) &&
+              mbar_wait_warp(smem_addr(&bar->st_full[0]), 0, wc);
+    if (ok) {
+      tc_fence_after();
+      sdp(0, sSt);
+      umma_commit_warp(smem_addr(&bar->s_full[0]));
+      sdp(1, sSt);
+      umma_commit_warp(smem_addr(&bar->s_full[1]));
+    }
     for (int t = 0; t < steps && ok; ++t) {
       const int st = t % L::kStages;
-      if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[st]), (t / L::kStages) & 1, wc))) break;
-      tc_fence_after();
       const uint32_t qb = sSt + st * L::kStageBytes;
-      const uint32_t dob = qb + L::kTileBytes;
-      ss_group(kColS, sK, qb);                                   // S^T = K Q_i^T
-      ss_group(kColDP, sV, dob);                                 // dP^T = V dO_i^T
-      umma_commit_warp(smem_addr(&bar->s_full));
-      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full), t & 1, wc))) break;
+      const bool next = t + 1 < steps;
+      const uint32_t qb1 = sSt + ((t + 1) % L::kStages) * L::kStageBytes;
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full[0]), t & 1, wc))) break;
       tc_fence_after();
-      // dV += P^T dO_i and dK += dS^T Q_i: A from TMEM (bf16 over S^T, dP^T),
-      // B = dO_i / Q_i as K x N with N = d contiguous.
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t bdo = sdesc_sw128(dob + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDV, tmem + kColS + packed_col(kk), bdo, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
+      acc(0, qb, t == 0);
+      if (next) {
+        if (!(ok = mbar_wait_warp(smem_addr(&bar->st_full[(t + 1) % L::kStages]), ((t + 1) / L::kStages) & 1, wc)))
+          break;
+        tc_fence_after();
+        sdp(0, qb1);
+        umma_commit_warp(smem_addr(&bar->s_full[0]));
       }
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint64_t bq = sdesc_sw128(qb + kk * 2048, L::kChunkBytes, 1024);
-        umma_ts_warp(tmem + kColDK, tmem + kColDP + packed_col(kk), bq, kIdescAcc, (t > 0 || kk > 0) ? 1u : 0u);
-      }
+      if (!(ok = mbar_wait_warp(smem_addr(&bar->p_full[1]), t & 1, wc))) break;
+      tc_fence_after();
+      acc(1, qb, false);
       umma_commit_warp(smem_addr(&bar->st_empty[st]));
+      if (next) {
+        sdp(1, qb1);
+        umma_commit_warp(smem_addr(&bar->s_full[1]));
+      }
     }
     umma_commit_warp(smem_addr(&bar->done));
     umma_commit_warp(smem_addr(&bar->mma_final));
     __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar->mma_final), 0, wc, true));
   } else {
     // -------------------------------------------------------- compute warps
-    const int quarter = warp & 3, h = warp >> 2;   // lane quarter, column half
+    const int quarter = warp & 3, w2 = warp >> 2;  // lane quarter, 32-column part of each half
     const int row = quarter * 32 + lane;          // TMEM lane = key within the tile
     const int key = kt * kTile + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int t = 0; t < steps; ++t) {
+    for (int t = 0; t < steps && ok; ++t) {
       int zq, qt;
       step_q(t, zq, qt);
       const int st = t % L::kStages;
       // The lse2 / D vectors of this step landed with the stage's tiles.
-      if (!mbar_wait_warp(smem_addr(&bar->st_full[st]), (t / L::kStages) & 1, wc) ||
-          !mbar_wait_warp(smem_addr(&bar->s_full), t & 1, wc)) {
+      if (!mbar_wait_warp(smem_addr(&bar->st_full[st]), (t / L::kStages) & 1, wc)) {
         ok = false;
         break;
       }
-      tc_fence_after();
       const float* lse2v = vec + (st * 2 + 0) * kTile;
       const float* dv = vec + (st * 2 + 1) * kTile;
       const int qbase = qt * kTile;
-      const bool need_mask = (CAUSAL && qt == kt) || (qbase + kTile > p.N);
-      // Row = key, column = query: P^T = 2^(s * scale * log2 e - lse2[q]),
-      // dS^T = P^T * (dP^T - D[q]); masked pairs (key > query, or a query
-      // past N) get P = 0.  P^T goes over S^T, dS^T over dP^T.
-      uint32_t dspk[32];
-      ATTN47_BWD_ROW_LOOP(tl + kColS, tl + kColDP, h, {
-        const int c = c2 * 2;
-        float pv[2];
-        float dsv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int qc = chunk * 32 + c + e;
-          const int q = qbase + qc;
-          const bool masked = need_mask && ((CAUSAL && key > q) || q >= p.N);
-          pv[e] = masked ? 0.f : ex2(__uint_as_float(ra[c + e]) * sl2 - lse2v[qc]);
-          dsv[e] = pv[e] * (__uint_as_float(rb[c + e]) - dv[qc]);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (!mbar_wait_warp(smem_addr(&bar->s_full[h]), t & 1, wc)) {
+          ok = false;
+          break;
         }
-        pk[sub * 16 + c2] = pack_bf16x2(pv[0], pv[1]);
-        dspk[sub * 16 + c2] = pack_bf16x2(dsv[0], dsv[1]);
-      })
-      ATTN47_TMEM_ST32(tl + kColDP + h * 64, dspk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bar->p_full));
+        tc_fence_after();
+        // Row = key, column = query: P^T = 2^(s * scale * log2 e - lse2[q]),
+        // dS^T = P^T * (dP^T - D[q]); masked pairs (key > query, or a query
+        // past N) get P = 0.  P^T goes over S_h^T, dS^T over dP_h^T; 32
+        // queries of half h per warp.
+        const uint32_t cs = col_s(h) + w2 * 32, cd = col_dp(h) + w2 * 32;
+        uint32_t ra[32], rb[32], pk[16], dspk[16];
+        ATTN47_TMEM_LD32(tl + cs, ra);
+        ATTN47_TMEM_LD32(tl + cd, rb);
+        ATTN47_TMEM_LD_WAIT(ra);
+        ATTN47_TMEM_LD_WAIT(rb);
+        // Queries qbase + c0 + c are allowed for lo <= c < hi (causal:
+        // query >= key; all: query < N); the exponential is formed for every
+        // query and the masked ones are then selected away (no branches).
+        const int c0 = h * 64 + w2 * 32;
+        const int lo = CAUSAL ? key - qbase - c0 : 0;
+        const int hi = p.N - qbase - c0;
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * c2 + e;
+            const int qc = c0 + c;
+            const float ev = ex2(__uint_as_float(ra[c]) * sl2 - lse2v[qc]);
+            pv[e] = (c >= lo && c < hi) ? ev : 0.f;
+            dsv[e] = pv[e] * (__uint_as_float(rb[c]) - dv[qc]);
+          }
+          pk[c2] = pack_bf16x2(pv[0], pv[1]);
+          dspk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        ATTN47_TMEM_ST16(tl + cs, pk);
+        ATTN47_TMEM_ST16(tl + cd, dspk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&bar->p_full[h]));
+      }
     }
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(smem_addr(&bar->done), 0, wc)) {
@@ -505,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float mul = which ? p.scale : 1.f;
         const uint32_t col = which ? kColDK : kColDV;
 #pragma unroll 1
-        for (int c0 = h * (D / 2); c0 < (h + 1) * (D / 2); c0 += 32) {
+        for (int c0 = w2 * (D / 2); c0 < (w2 + 1) * (D / 2); c0 += 32) {
           uint32_t o[32];
           ATTN47_TMEM_LD32(tl + col + c0, o);
           ATTN47_TMEM_LD_WAIT(o);

@@ -273,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Lt = DecLayout<D, GM>;
   constexpr int kStages = Lt::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_align1024(smem_raw);
   DecShared* sh = reinterpret_cast<DecShared*>(smem + Lt::kOffShared);
   const uint32_t ring = smem_addr(smem);
   const uint32_t qring = smem_addr(smem + Lt::kOffQ);

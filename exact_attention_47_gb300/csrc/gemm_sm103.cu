@@ -52,17 +52,13 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 __device__ __forceinline__ float silu(float g) { return g / (1.f + __expf(-g)); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     swiglu_proj_kernel(const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap tw,
                        const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   GemmBars* bar = reinterpret_cast<GemmBars*>(smem + kOffBar);
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

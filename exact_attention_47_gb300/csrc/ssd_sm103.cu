@@ -38,10 +38,6 @@ constexpr int kHeadsPerOut = 16;       // heads of one group per output CTA
 constexpr int kRows = 64;              // tokens per TMA box of x and B
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-
 // x <- bf16(x * w) for the 8 bf16 values of one 16-byte piece, on packed
 // bf16 pairs: w = w_hi + w_lo with both parts bf16, and
 // x w = fma(x, w_hi, x w_lo) rounded once; the error of the small term
@@ -110,7 +106,7 @@ __global__ void __launch_bounds__(192, 1)
   using Lt = StateLayout<N, Q>;
   constexpr int S = Lt::kStages;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   StateBars* bar = reinterpret_cast<StateBars*>(smem + Lt::kOffBar);
   float* ws = reinterpret_cast<float*>(smem + Lt::kOffW);
   float* gl = reinterpret_cast<float*>(smem + Lt::kOffGl);
@@ -460,7 +456,7 @@ __global__ void __launch_bounds__(320, 1)
                    const SsdParams p) {
   using Lt = OutLayout<N, Q>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  uint8_t* smem = smem_align1024(smem_raw);
   OutBars* bar = reinterpret_cast<OutBars*>(smem + Lt::kOffBar);
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
