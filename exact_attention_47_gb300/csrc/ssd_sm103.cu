@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(192, 1)
           const int i = lane * E + e;
           const float gv = (v[e] + offset) * kLog2e;
           gw[i] = gv;
-          wrow[i] = i < n_len ? ex2(g_last - gv) : 0.f;
+          const float wv = ex2(g_last - gv);
+          wrow[i] = i < n_len ? wv : 0.f;
         }
         if (lane == 0) gl[ssel] = g_last;
       }
@@ -682,12 +683,14 @@ __global__ void __launch_bounds__(320, 1)
           const float* gk = gsm + JO + sb * 32;
           if (sb == wq) {
             ATTN47_TMEM_LD_WAIT(v);
+            // Keys sb*32 + c are allowed for c <= r - sb*32; the weight is
+            // formed for every key and the masked ones are selected away.
+            const int lim = r - sb * 32;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int j = sb * 32 + 2 * e;
-              const float p0 = j <= r ? __uint_as_float(v[2 * e]) * ex2(gi - gk[2 * e]) : 0.f;
-              const float p1 = j + 1 <= r ? __uint_as_float(v[2 * e + 1]) * ex2(gi - gk[2 * e + 1]) : 0.f;
-              w[e] = pack_bf16x2(p0, p1);
+              const float w0 = __uint_as_float(v[2 * e]) * ex2(gi - gk[2 * e]);
+              const float w1 = __uint_as_float(v[2 * e + 1]) * ex2(gi - gk[2 * e + 1]);
+              w[e] = pack_bf16x2(2 * e <= lim ? w0 : 0.f, 2 * e + 1 <= lim ? w1 : 0.f);
             }
           } else {
             // Split at the sub-block's last key m: row factor 2^(g_i - g_m),
