@@ -138,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tv, const FwdParams p) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_align1024(smem_raw);
+  // Aligned through an integer round trip (the pointer becomes generic):
+  // measured faster for this kernel than smem_align1024.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   FwdBarriers* bar = reinterpret_cast<FwdBarriers*>(smem + L::kOffBar);
   const uint32_t sQ = smem_addr(smem + L::kOffQ);
   const uint32_t sK = smem_addr(smem + L::kOffK);
