@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     fused_swiglu,
     library_path,
     load_library,
+    selftest_exp2_poly,
     selftest_wait_timeout,
     set_decode_max_ctas,
     set_wait_timeout_ns,

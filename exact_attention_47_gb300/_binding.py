@@ -46,6 +46,7 @@ _SIGS = {
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_selftest_exp2_poly": (_I, [_P, _P, _I, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_abi_version": (_I, []),
@@ -415,6 +416,15 @@ def set_wait_timeout_ns(ns):
 def set_decode_max_ctas(ctas):
     """Cap the CTAs of a decode launch (0: one full wave)."""
     load_library().attn_set_decode_max_ctas(int(ctas))
+
+
+def selftest_exp2_poly(x, y=None, stream=None):
+    """y = 2^x (fp32 CUDA tensors) by the forward softmax's FMA-pipe exp2."""
+    _need_cuda("x", x, torch.float32)
+    dev = x.device
+    y = _output("y", y, x.shape, torch.float32, dev)
+    _call("attn_selftest_exp2_poly", dev, _ptr(x), _ptr(y), x.numel(), _stream_handle(stream, dev))
+    return y
 
 
 def selftest_wait_timeout(timeout_ns, stream=None):

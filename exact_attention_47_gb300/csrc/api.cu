@@ -880,6 +880,44 @@ attn_status_t attn_get_device_status(void* stream, unsigned int* flags_out) {
   return ATTN_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// One thread per pair of inputs: y = 2^x by the forward softmax's FMA-pipe
+// exp2 (ex2_poly2), for testing that function on the device.
+__global__ void selftest_exp2_poly_kernel(const float* x, float* y, int n) {
+  const long long i = 2LL * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const bool two = i + 1 < n;
+  float r0, r1;
+  attn47::f2_unpack(attn47::ex2_poly2(attn47::f2_pack(x[i], two ? x[i + 1] : 0.f)), r0, r1);
+  y[i] = r0;
+  if (two) y[i + 1] = r1;
+}
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_selftest_exp2_poly(const float* x, float* y, int n, void* stream) {
+  if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be >= 0");
+  if (n == 0) {
+    g_last_error[0] = '\0';
+    return ATTN_OK;
+  }
+  if (!x || !y) return fail(ATTN_ERR_INVALID_ARG, "x and y must be non-null");
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) || (reinterpret_cast<uintptr_t>(y) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "x and y must be 4-byte aligned");
+  DeviceInfo* dev = nullptr;
+  attn_status_t st = current_device(&dev);
+  if (st != ATTN_OK) return st;
+  const size_t bytes = static_cast<size_t>(n) * 4;
+  if ((st = check_bufs(*dev, {{x, bytes, "x"}, {y, bytes, "y"}})) != ATTN_OK) return st;
+  const long long pairs = (static_cast<long long>(n) + 1) / 2;
+  selftest_exp2_poly_kernel<<<static_cast<unsigned>((pairs + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, y, n);
+  return launch_result(cudaGetLastError(), "attn_selftest_exp2_poly");
+}
+
 attn_status_t attn_selftest_wait_timeout(unsigned long long timeout_ns, void* stream,
                                          unsigned int* flags_out) {
   if (!flags_out) return fail(ATTN_ERR_INVALID_ARG, "flags_out must be non-null");

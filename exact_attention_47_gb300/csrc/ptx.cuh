@@ -63,6 +63,45 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// exp2 of a pair of floats on the FMA pipe instead of the special-function
+// unit (so the two could share a softmax's exponentials; measured slower
+// in the forward on GB300, whose softmax loop is issue-bound, so only the
+// self-test entry point uses it): with n = round(x)
+// and f = x - n in [-1/2, 1/2], 2^x = 2^n 2^f; 2^f is a degree-4 polynomial
+// (coefficients from exp2_poly_fit.py: relative error 2.7e-6, under 2^-18,
+// in fp32 Horner form), and 2^n is added to its exponent field.  n comes
+// from the round-to-nearest of x + 1.5 * 2^23, whose low bits hold n; their
+// shift by 23 adds n to the exponent (the constant's own bits shift out).
+// Inputs are clamped to [-126, 127]: below -126 the result is a tiny value
+// below 2^-125 (not 0); -inf gives that too.
+constexpr float kEx2C0 = 9.999992847e-01f, kEx2C1 = 6.931217909e-01f, kEx2C2 = 2.402470261e-01f,
+                kEx2C3 = 5.591800436e-02f, kEx2C4 = 9.571807459e-03f;
+__device__ __forceinline__ uint64_t ex2_poly2(uint64_t x2) {
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  x0 = fminf(fmaxf(x0, -126.f), 127.f);
+  x1 = fminf(fmaxf(x1, -126.f), 127.f);
+  const uint64_t xc = f2_pack(x0, x1);
+  const uint64_t magic = f2_pack(0x1.8p23f, 0x1.8p23f);
+  const uint64_t t = f2_add(xc, magic);
+  const uint64_t f = f2_sub(xc, f2_sub(t, magic));
+  uint64_t q = f2_fma(f2_pack(kEx2C4, kEx2C4), f, f2_pack(kEx2C3, kEx2C3));
+  q = f2_fma(q, f, f2_pack(kEx2C2, kEx2C2));
+  q = f2_fma(q, f, f2_pack(kEx2C1, kEx2C1));
+  q = f2_fma(q, f, f2_pack(kEx2C0, kEx2C0));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  return f2_pack(__uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23)),
+                 __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23)));
+}
+
 // c + (float) of the low / high bf16 half of w, in one mixed-precision add
 // (sm_100+): the rounded numerators summed exactly as the MMA sees them.
 __device__ __forceinline__ float add_bf16lo_f32(uint32_t w, float c) {

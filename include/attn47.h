@@ -412,6 +412,22 @@ void attn_set_wait_timeout_ns(unsigned long long ns);
 void attn_set_decode_max_ctas(int ctas);
 
 /*
+ * attn_selftest_exp2_poly — y[i] = 2^x[i] by an exp2 on the FMA pipe
+ * instead of the special-function unit, the building block for moving part
+ * of a softmax's exponentials off that unit ("Accelerating Mamba-2 with
+ * high-performance forward kernels in NVIDIA CUDA Tile" works in exp2 for
+ * the same unit's sake).  On GB300 the forward softmax measured slower with
+ * it (its loop is limited by instruction issue, not by that unit), so the
+ * kernels do not use it; this entry keeps it tested.
+ * 2^x = 2^round(x) * p(x - round(x)), p a degree-4 polynomial with relative
+ * error below 2^-18 on [-1/2, 1/2].  x is clamped to [-126, 127] first
+ * (below -126 the result is a tiny value under 2^-125, not 0).  For tests:
+ * x and y are device arrays of n floats (4-byte aligned, may not overlap
+ * except x == y); one kernel on `stream`, nothing synchronised.
+ */
+attn_status_t attn_selftest_exp2_poly(const float* x, float* y, int n, void* stream);
+
+/*
  * attn_selftest_wait_timeout — launches a one-warp kernel that waits on a
  * shared-memory barrier that nothing will ever complete, with the given time
  * limit, so the bounded-wait path can be tested without hanging or faulting

@@ -129,6 +129,13 @@ def test_swiglu_projection_host_validation(lib):
     assert lib.swiglu_projection(FAKE, FAKE, FAKE, 0, 64, 128, None) == OK
 
 
+def test_selftest_exp2_poly_host_validation(lib):
+    assert lib.attn_selftest_exp2_poly(FAKE, FAKE, -1, None) == INVALID
+    assert lib.attn_selftest_exp2_poly(None, FAKE, 4, None) == INVALID
+    assert lib.attn_selftest_exp2_poly(FAKE, ctypes.c_void_p(0x10002), 4, None) == INVALID   # misaligned
+    assert lib.attn_selftest_exp2_poly(FAKE, FAKE, 0, None) == OK
+
+
 def _ssd(lib, batch=2, L=100, H=8, G=1, P=64, N=128, chunk=64, ws_bytes=None):
     need = lib.ssd_workspace_size(batch, L, H, N, chunk)
     return lib.ssd_chunked_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, batch, L, H, G, P, N,
