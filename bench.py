@@ -64,12 +64,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = os.path.join(ROOT, "exact_attention_47_gb300", "csrc")
 TRAFFIC = {
     # median read + median write of 3 launches
-    "fwd": {"bytes": 67195136 + 5155072, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
-            "sha256": "c34e733b18ef16ed00df4bf8aab02bb3a237eb07e9774a402cd207357f993b6f"},
+    "fwd": {"bytes": 67206400 + 5443840, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
+            "sha256": "644d0ed526136e30fd1a072177aa5d3e1af87c7ec15dc54c11a86248f6a9f82f"},
     # decode kernel + merge kernel, medians of 3 launches each
-    "dec": {"bytes": (132293888 + 228096) + (3272192 + 0),
+    "dec": {"bytes": (132314880 + 155904) + (3272448 + 0),
             "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
-            "sha256": "1ee64ce39e977a55269b55a183e6ea9a65b79ec848a19c579892b982a2a7cbaf"},
+            "sha256": "9f956a58af15c700fd216f5ab29ad5b9fdfc5766bb31c165da71a83a4200254e"},
 }
 
 
