@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     load_library,
     selftest_exp2_poly,
     selftest_wait_timeout,
+    set_decode_early_plan,
     set_decode_max_ctas,
     set_wait_timeout_ns,
     ssd_chunked_fwd,

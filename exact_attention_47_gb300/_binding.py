@@ -45,6 +45,7 @@ _SIGS = {
     "attn_get_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (None, [ctypes.c_ulonglong]),
     "attn_set_decode_max_ctas": (None, [_I]),
+    "attn_set_decode_early_plan": (None, [_I]),
     "attn_selftest_wait_timeout": (_I, [ctypes.c_ulonglong, _P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_selftest_exp2_poly": (_I, [_P, _P, _I, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -416,6 +417,13 @@ def set_wait_timeout_ns(ns):
 def set_decode_max_ctas(ctas):
     """Cap the CTAs of a decode launch (0: one full wave)."""
     load_library().attn_set_decode_max_ctas(int(ctas))
+
+
+def set_decode_early_plan(on):
+    """Let later decode calls read seq_lens and block_table before the
+    preceding kernel in the stream has finished (the caller guarantees that
+    kernel writes neither)."""
+    load_library().attn_set_decode_early_plan(1 if on else 0)
 
 
 def selftest_exp2_poly(x, y=None, stream=None):

@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -45,6 +47,20 @@ attn_status_t fail(attn_status_t s, const char* fmt, ...) {
 unsigned long long g_timeout_ns = 1000000000ull;
 
 int g_decode_max_ctas = 0;  // 0 = one full wave
+std::atomic<bool> g_decode_early_plan{false};
+
+// Tags of the decode's per-run arrival counters: a different nonzero value
+// for every call of this process, starting from a clock-derived value so
+// that workspace contents left by another process are unlikely to carry it.
+unsigned int next_decode_epoch() {
+  static std::atomic<unsigned int> epoch{static_cast<unsigned int>(
+      std::chrono::steady_clock::now().time_since_epoch().count() * 2654435761ull)};
+  unsigned int e;
+  do {
+    e = epoch.fetch_add(1u) + 1u;
+  } while (e == 0u);
+  return e;
+}
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -291,6 +307,8 @@ attn_status_t decode_launch(const DeviceInfo& dev, const void* q, const void* k_
   a.num_blocks = num_blocks;
   a.sms = dev.sms;
   a.max_ctas = g_decode_max_ctas;
+  a.early_plan = g_decode_early_plan.load();
+  a.epoch = next_decode_epoch();
   a.scale = scale;
   a.status = dev.status;
   a.timeout_ns = g_timeout_ns;
@@ -335,6 +353,8 @@ const char* attn_status_string(attn_status_t s) {
 void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns < 1000ull ? 1000ull : ns; }
 
 void attn_set_decode_max_ctas(int ctas) { g_decode_max_ctas = ctas > 0 ? ctas : 0; }
+
+void attn_set_decode_early_plan(int on) { g_decode_early_plan.store(on != 0); }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {

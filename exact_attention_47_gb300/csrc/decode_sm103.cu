@@ -26,8 +26,16 @@
 //               segment's end the seven warp states are merged in shared
 //               memory
 // A segment that covers a whole sequence writes O and LSE directly; the
-// others write an unnormalised partial (O, max, sum), and a second kernel
-// (launched as a programmatic dependent) merges the parts of each sequence.
+// others publish an unnormalised partial (O, max, sum) and count their
+// arrival on the run's counter; the part that arrives last merges all parts
+// of the run (exactly, with their maxima) and writes O and LSE.
+//
+// The kernel is launched as a programmatic dependent of the work before it
+// in the stream: its CTAs start while that work drains and wait for it
+// (griddepcontrol.wait) before touching anything it may write.  With the
+// early plan on, the wait comes after the split plan and the first table
+// translations, which then read seq_lens and the block table before the
+// preceding kernel has finished.
 #include <cuda_runtime.h>
 
 #include "decode_sm103.h"
@@ -115,8 +123,10 @@ struct DecParams {
   float* lse;
   float* ws_o;
   float* ws_ml;
-  int* nparts;                    // parts per (sequence, KV head), for the merge kernel
+  unsigned long long* arrive;      // arrival counter per (sequence, KV head): tag << 32 | parts arrived
   int num_seqs, Hq, Hkv, group, max_blocks, num_blocks, max_parts;
+  unsigned int epoch;              // this call's tag (never 0)
+  int early_plan;                  // plan before waiting for the preceding kernel
   float scale_log2;
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -182,28 +192,162 @@ struct SegWalk {
   }
 };
 
+// Arrival of one part of a split run on the run's counter (one lane).  The
+// counter holds this call's tag in its high half and the parts arrived in
+// its low half; a value with another tag (a previous call, or workspace
+// contents never written by this library) counts as zero arrivals.  Returns
+// whether this was the last part; the last part resets the counter to zero
+// for the next call (a replayed graph reuses its tag).  The first guess of
+// the counter's value is what the usual order of arrivals gives: part 0 is
+// the last segment of its CTA and arrives after the others.
+__device__ __forceinline__ bool arrive_part(const DecParams& p, unsigned long long* slot, int part,
+                                            int nparts) {
+  const unsigned long long tag = static_cast<unsigned long long>(p.epoch) << 32;
+  unsigned long long cur = part == 0 ? tag | static_cast<unsigned int>(nparts - 1) : 0ull;
+  for (int i = 0; i < 2 * nparts + 2; ++i) {
+    const unsigned long long base = (cur >> 32) == p.epoch ? cur : tag;
+    const unsigned long long next = base + 1;
+    const unsigned long long prev = atomicCAS(slot, cur, next);
+    if (prev == cur) {
+      const bool last = static_cast<int>(next & 0xffffffffu) >= nparts;
+      if (last) atomicExch(slot, 0ull);
+      return last;
+    }
+    cur = prev;
+  }
+  atomicOr(p.status, kDevTimeout);   // more arrivals than parts: cannot happen
+  return false;
+}
+
+// Exact merge of the published parts [s0, s1) of the G query heads
+// hq0 .. hq0+G-1 by one warp: with M = max_s m_s, O = sum_s 2^(m_s - M) O_s
+// / sum_s 2^(m_s - M) l_s and LSE = (M + log2 of the denominator) ln 2.
+// Rows go in groups of 8 and parts two at a time (every load of a pass
+// issued before any is used) with a running maximum.  Lane l owns columns
+// [l D/32, (l + 1) D/32) of every row; lane j < 16 holds the (max, sum) of
+// part s + j % 2 of row j / 2 of the group.  Every part is read back from
+// the workspace, so the result does not depend on which part merges.
+template <int D>
+__device__ __forceinline__ void merge_published_parts(const DecParams& p, size_t hq0, int G, int s0, int s1,
+                                                      int lane) {
+  constexpr int E = D / 32;
+  constexpr int RG = 8, CH = 2;
+  const size_t mp = static_cast<size_t>(p.max_parts);
+  for (int g0 = 0; g0 < G; g0 += RG) {
+    const int rows = min(RG, G - g0);
+    const size_t h0 = hq0 + g0;
+    const int jr = min(lane / CH, rows - 1);
+    const int jt = lane % CH;
+    const bool jrow = lane / CH < rows;
+    float Mrun = -INFINITY, Lrun = 0.f;
+    float acc[RG][E];
+#pragma unroll
+    for (int r = 0; r < RG; ++r)
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
+    for (int s = s0; s < s1; s += CH) {
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (jrow && s + jt < s1)
+        ml = __ldcg(reinterpret_cast<const float2*>(p.ws_ml) + (h0 + jr) * mp + s + jt);
+      float v[CH][RG][E];
+#pragma unroll
+      for (int t = 0; t < CH; ++t)
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+          const size_t slot = (h0 + min(r, rows - 1)) * mp + min(s + t, s1 - 1);
+          const float* src = p.ws_o + slot * D + lane * E;
+          if constexpr (E == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+            v[t][r][0] = x.x;
+            v[t][r][1] = x.y;
+            v[t][r][2] = x.z;
+            v[t][r][3] = x.w;
+          } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+            v[t][r][0] = x.x;
+            v[t][r][1] = x.y;
+          }
+        }
+      const float cm = fmaxf(ml.x, __shfl_xor_sync(0xffffffffu, ml.x, 1));
+      const float Mn = fmaxf(Mrun, cm);
+      const float a = Mn == -INFINITY ? 1.f : ex2(Mrun - Mn);
+      const float w = ml.x == -INFINITY ? 0.f : ex2(ml.x - Mn);
+      float lw = w * ml.y;
+      lw += __shfl_xor_sync(0xffffffffu, lw, 1);
+      Lrun = Lrun * a + lw;
+      Mrun = Mn;
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        const float ar = __shfl_sync(0xffffffffu, a, r * CH);
+        const float w0 = __shfl_sync(0xffffffffu, w, r * CH);
+        const float w1 = __shfl_sync(0xffffffffu, w, r * CH + 1);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[r][e] = acc[r][e] * ar + w0 * v[0][r][e] + w1 * v[1][r][e];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      if (r >= rows) break;
+      const float L = __shfl_sync(0xffffffffu, Lrun, r * CH);
+      const float M = __shfl_sync(0xffffffffu, Mrun, r * CH);
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const size_t hq = h0 + r;
+      if constexpr (E == 4) {
+        uint2 pk;
+        pk.x = pack_bf16x2(acc[r][0] * inv, acc[r][1] * inv);
+        pk.y = pack_bf16x2(acc[r][2] * inv, acc[r][3] * inv);
+        *reinterpret_cast<uint2*>(p.o + hq * D + lane * E) = pk;
+      } else {
+        *reinterpret_cast<uint32_t*>(p.o + hq * D + lane * E) = pack_bf16x2(acc[r][0] * inv, acc[r][1] * inv);
+      }
+      if (lane == 0 && p.lse != nullptr) p.lse[hq] = L > 0.f ? (M + __log2f(L)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+// Parts of the (sequence, KV head) run whose blocks at cost positions
+// pcost + kRunCost .. pcost + kRunCost + nblk - 1 are split over the CTAs
+// (CTA x holds [x chunk, (x + 1) chunk)): their count, and this CTA's index.
+struct RunParts {
+  int nparts, part;
+  __device__ RunParts(int pcost, int nblk, int chunk) {
+    const int first_cta = (pcost + kRunCost) / chunk;
+    nparts = (pcost + kRunCost + nblk - 1) / chunk - first_cta + 1;
+    part = static_cast<int>(blockIdx.x) - first_cta;
+  }
+};
+
+// O = 0 and LSE = -inf for the empty sequences b = blockIdx.x, + gridDim.x,
+// ... (one warp).
+template <int D>
+__device__ __forceinline__ void write_empty_sequences(const DecParams& p, const int* nb_cache, int lane) {
+  for (int b = blockIdx.x; b < p.num_seqs; b += gridDim.x) {
+    if (seq_blocks(p, nb_cache, b) != 0) continue;
+    __nv_bfloat16* dst = p.o + static_cast<size_t>(b) * p.Hq * D;
+    for (int i = lane; i < p.Hq * D / 2; i += 32) reinterpret_cast<uint32_t*>(dst)[i] = 0u;
+    for (int h = lane; h < p.Hq; h += 32)
+      if (p.lse != nullptr) p.lse[static_cast<size_t>(b) * p.Hq + h] = -INFINITY;
+  }
+}
+
 // Merge of one segment by one warp: the seven consumer warps' states of the
 // segment (rows < G of the merge buffer) combined into O and the LSE when the
-// segment is a whole run, else into this CTA's partial of the run, and the
-// run's part count recorded by the holder of part 0 for the merge kernel.
+// segment is a whole run, else into this CTA's partial of the run, published
+// and counted; the last part of the run to arrive merges all of its parts.
 // Lane l owns columns [l D/32, (l + 1) D/32).
 template <int D, int GM>
 __device__ __forceinline__ void merge_segment(const DecParams& p, const float* cbo, const float* cbm,
                                               const SegWalk& w, int chunk, int G, int lane) {
   constexpr int E = D / 32;
-  // The run's parts are the CTAs holding its blocks, cost positions
-  // pcost + kRunCost .. pcost + kRunCost + nblk - 1 (CTA x holds
-  // [x chunk, (x + 1) chunk)); this CTA's part index counts from the first.
-  const int first_cta = (w.pcost + kRunCost) / chunk;
-  const int nparts = (w.pcost + kRunCost + w.nblk - 1) / chunk - first_cta + 1;
-  const int part = static_cast<int>(blockIdx.x) - first_cta;
+  const RunParts rp(w.pcost, w.nblk, chunk);
+  const int nparts = rp.nparts, part = rp.part;
   const bool whole = nparts == 1;
   const bool in_range = part >= 0 && part < nparts && nparts <= p.max_parts;
   const size_t hq0 = static_cast<size_t>(w.b) * p.Hq + w.g * G;
 #pragma unroll
   for (int r = 0; r < GM; ++r) {
     if (r >= G) break;
-    // Every lane reads the seven (max, sum) pairs of the row (shared-memory
+    // Every lane reads the (max, sum) pairs of the row (shared-memory
     // broadcasts) and forms the weights itself: no cross-lane chains, and
     // the rows are independent of each other.
     float mw[kConsumers], M = -INFINITY;
@@ -258,11 +402,22 @@ __device__ __forceinline__ void merge_segment(const DecParams& p, const float* c
       }
     }
   }
-  // The holder of part 0 records the run's part count for the merge kernel
-  // (1: the run was written here, nothing to merge).
-  if (part == 0 && lane == 0) {
-    p.nparts[static_cast<size_t>(w.b) * p.Hkv + w.g] = (whole || !in_range) ? 1 : nparts;
-    if (!in_range) atomicOr(p.status, kDevTimeout);   // cannot happen: the split bounds nparts
+  if (whole) return;
+  if (!in_range) {
+    if (lane == 0) atomicOr(p.status, kDevTimeout);   // cannot happen: the split bounds nparts
+    return;
+  }
+  unsigned long long* slot = p.arrive + static_cast<size_t>(w.b) * p.Hkv + w.g;
+  // Publish this part (every lane's writes visible to the whole GPU before
+  // the arrival is counted), then count it.
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = arrive_part(p, slot, part, nparts);
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (last) {
+    __threadfence();
+    merge_published_parts<D>(p, hq0, G, 0, nparts, lane);
   }
 }
 
@@ -308,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_share(p.block_table, static_cast<size_t>(p.num_seqs) * p.max_blocks * 4);
     prefetch_share(p.q, static_cast<size_t>(p.num_seqs) * p.Hq * D * 2);
   }
+  // Without the early plan nothing is read before the preceding kernel has
+  // finished (the L2 prefetches above are hints only).
+  if (!p.early_plan) pdl_wait_primary();
   if (warp == kConsumers) {
     int T = 0, C = 0;
     bool bad = false;
@@ -414,7 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   const int c0 = sh->c0, c1 = sh->c1, chunk = sh->chunk, b0 = sh->b0, off0 = sh->off0;
   const int pseq0 = sh->pseq0;
-  if (c0 >= c1 || b0 < 0) return;                 // whole CTA: no work
+  if (c0 >= c1 || b0 < 0) {                       // whole CTA: no work
+    if (warp == kConsumers) {
+      pdl_wait_primary();
+      write_empty_sequences<D>(p, nb_cache, lane);
+    }
+    return;
+  }
   const WaitCtl wc{&sh->abort, p.status, p.timeout_ns};
 
   if (warp == kConsumers) {
@@ -448,7 +612,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fetch(lane, cur_ph, cur_b, cur_g);
     fetch(32 + lane, n1_ph, n1_b, n1_g);
     fetch(64 + lane, n2_ph, n2_b, n2_g);
+    // Everything from here on may read what the preceding kernel wrote (the
+    // queries, the newest cache slots) or write what it reads.
+    pdl_wait_primary();
 
+    // Every cached K/V byte is read once: keep it from evicting the
+    // published parts and arrival counters that other CTAs read back.
+    const uint64_t stream_policy = l2_policy_evict_first();
     int seg = 0, carry_b = -1, carry_g = -1;
     bool ok = true;
     const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
@@ -498,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rowk = (cur_ph * p.Hkv + cur_g) * kBS;
               const uint32_t dst = ring + st * Lt::kStage;
               mbar_arrive_expect_tx(fb, Lt::kStage);
-              tma_load_3d(dst, &tk, fb, 0, rowk, 0);
-              tma_load_3d(dst + Lt::kHalf, &tv, fb, 0, rowk, 0);
+              tma_load_3d_hint(dst, &tk, fb, 0, rowk, 0, stream_policy);
+              tma_load_3d_hint(dst + Lt::kHalf, &tv, fb, 0, rowk, 0, stream_policy);
             } else {
               mbar_arrive(fb);
             }
@@ -519,8 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fetch(base + 96 + lane, n2_ph, n2_b, n2_g);
     }
     __syncwarp();
-    // Every copy is issued: the merge kernel may launch (it waits for this
-    // grid to finish before reading).
+    // Every copy is issued: the next kernel in the stream may launch its
+    // CTAs (it waits for this grid to finish before using its results).
     pdl_launch_dependents();
     // Every copy issued must have landed before the CTA may exit: wait for
     // the last fill of every stage and query slot.
@@ -532,8 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int fills = sh->qfills[lane];
       if (fills > 0) mbar_wait(smem_addr(&sh->qfull[lane]), (fills - 1) & 1, wc, true);
     }
+    write_empty_sequences<D>(p, nb_cache, lane);
   } else {
     // ----------------------------------------------------------- consumers
+    pdl_wait_primary();
     const float sl2 = p.scale_log2;
     const int r0 = lane >> 2;               // fragment row (query head within the group)
     const int cq = (lane & 3) * 2;          // fragment column pair
@@ -739,109 +911,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
 }
 
-struct CombineParams {
-  const int* seq_lens;
-  const float* ws_o;
-  const float* ws_ml;
-  const int* nparts;
-  __nv_bfloat16* o;
-  float* lse;
-  int Hq, Hkv, max_blocks, max_parts;
-};
-
-// One warp per (sequence, query head): exact merge of the parts of a
-// sequence that was split over several CTAs.  Everything the merge can need
-// is loaded at once, before any of it is used: the length, the part count,
-// every part's (max, sum) (lane s holds part s) and the O rows of the first
-// kPrefetch parts; the part count then selects among them (rows of parts
-// that were not written are never read into the sum).  So a merge costs one
-// round trip to memory; only sequences with more parts loop over the rest.
-// Sequences with one part were written by the decode kernel; empty
-// sequences get O = 0 and LSE = -inf here.
-constexpr int kPrefetch = 8;
-template <int D>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const CombineParams p) {
-  pdl_wait_primary();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 4 + warp;
-  const int b = blockIdx.y;
-  if (h >= p.Hq) return;
-  const int G = p.Hq / p.Hkv;
-  const size_t base = (static_cast<size_t>(b) * p.Hq + h) * p.max_parts;
-  // ---- all independent loads first
-  const int L_raw = p.seq_lens[b];
-  const int np_raw = __ldcg(p.nparts + b * p.Hkv + h / G);
-  float m_lane = -INFINITY, l_lane = 0.f;
-  if (lane < p.max_parts) {
-    m_lane = __ldcg(p.ws_ml + (base + lane) * 2);
-    l_lane = __ldcg(p.ws_ml + (base + lane) * 2 + 1);
-  }
-  float v[kPrefetch][D / 32];
-#pragma unroll
-  for (int s = 0; s < kPrefetch; ++s) {
-    const float* src = p.ws_o + (base + min(s, p.max_parts - 1)) * D;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) v[s][e] = __ldcg(src + lane + 32 * e);
-  }
-  // ---- then decide
-  const int L = L_raw < 0 ? 0 : min(L_raw, p.max_blocks * kBS);
-  __nv_bfloat16* dst = p.o + (static_cast<size_t>(b) * p.Hq + h) * D;
-  if (L == 0) {
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(0.f);
-    if (lane == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(b) * p.Hq + h] = -INFINITY;
-    return;
-  }
-  const int np = min(np_raw, p.max_parts);
-  if (np <= 1) return;
-  if (lane >= np) {
-    m_lane = -INFINITY;
-    l_lane = 0.f;
-  }
-  // Parts beyond 32 (only with very long block tables) join the maximum here.
-  for (int s = 32 + lane; s < np; s += 32) m_lane = fmaxf(m_lane, __ldcg(p.ws_ml + (base + s) * 2));
-  float M = m_lane;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float acc[D / 32];
-#pragma unroll
-  for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
-  float lsum = 0.f;
-  if (M != -INFINITY) {
-    // Weights of the first 32 parts from the values already in registers.
-    const float w = (lane < np) ? ex2(m_lane - M) : 0.f;
-    float lw = w * l_lane;
-#pragma unroll
-    for (int s = 0; s < kPrefetch; ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      if (s < np)
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e) acc[e] += ws * v[s][e];
-    }
-    for (int s = kPrefetch; s < min(np, 32); ++s) {
-      const float ws = __shfl_sync(0xffffffffu, w, s);
-      const float* src = p.ws_o + (base + s) * D;
-#pragma unroll
-      for (int e = 0; e < D / 32; ++e) acc[e] += ws * __ldcg(src + lane + 32 * e);
-    }
-    for (int s = 32; s < np; ++s) {
-      const float ws = ex2(__ldcg(p.ws_ml + (base + s) * 2) - M);
-      if (lane == 0) lw += ws * __ldcg(p.ws_ml + (base + s) * 2 + 1);
-      const float* src = p.ws_o + (base + s) * D;
-#pragma unroll
-      for (int e = 0; e < D / 32; ++e) acc[e] += ws * __ldcg(src + lane + 32 * e);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-    lsum = lw;
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-#pragma unroll
-  for (int e = 0; e < D / 32; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
-  if (lane == 0 && p.lse != nullptr)
-    p.lse[static_cast<size_t>(b) * p.Hq + h] = lsum > 0.f ? (M + __log2f(lsum)) * kLn2 : -INFINITY;
-}
-
 template <int D, int GM>
 cudaError_t launch_t(const DecLaunch& a) {
   using Lt = DecLayout<D, GM>;
@@ -855,7 +924,7 @@ cudaError_t launch_t(const DecLaunch& a) {
   const int max_parts = decode_max_parts(a.max_blocks);
   float* ws_o = a.workspace;
   float* ws_ml = ws_o + static_cast<size_t>(a.num_seqs) * a.Hq * max_parts * D;
-  int* nparts = reinterpret_cast<int*>(ws_ml + static_cast<size_t>(a.num_seqs) * a.Hq * max_parts * 2);
+  auto* arrive = reinterpret_cast<unsigned long long*>(ws_ml + static_cast<size_t>(a.num_seqs) * a.Hq * max_parts * 2);
   DecParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.k_cache = reinterpret_cast<const __nv_bfloat16*>(a.k_cache);
@@ -866,7 +935,7 @@ cudaError_t launch_t(const DecLaunch& a) {
   p.lse = a.lse;
   p.ws_o = ws_o;
   p.ws_ml = ws_ml;
-  p.nparts = nparts;
+  p.arrive = arrive;
   p.num_seqs = a.num_seqs;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -874,42 +943,25 @@ cudaError_t launch_t(const DecLaunch& a) {
   p.max_blocks = a.max_blocks;
   p.num_blocks = a.num_blocks;
   p.max_parts = max_parts;
+  p.epoch = a.epoch;
+  p.early_plan = a.early_plan ? 1 : 0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
   // One wave: every CTA resident at once, each with an equal chunk.
   int ctas = a.sms * per_sm;
   if (a.max_ctas > 0 && ctas > a.max_ctas) ctas = a.max_ctas;
-  kern<<<static_cast<unsigned>(ctas), kThreads, Lt::kSmem, a.stream>>>(*a.tk, *a.tv, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  CombineParams c;
-  c.seq_lens = a.seq_lens;
-  c.ws_o = ws_o;
-  c.ws_ml = ws_ml;
-  c.nparts = nparts;
-  c.o = reinterpret_cast<__nv_bfloat16*>(a.o);
-  c.lse = a.lse;
-  c.Hq = a.Hq;
-  c.Hkv = a.Hkv;
-  c.max_blocks = a.max_blocks;
-  c.max_parts = max_parts;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Hq + 3) / 4, a.num_seqs);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Lt::kSmem;
   cfg.stream = a.stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Same shared-memory carveout as the decode kernel, so that the SMs need
-  // no reconfiguration between the two (or before the next decode).
-  e = cudaFuncSetAttribute(attn_decode_combine_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  e = cudaLaunchKernelEx(&cfg, attn_decode_combine_kernel<D>, c);
+  e = cudaLaunchKernelEx(&cfg, kern, *a.tk, *a.tv, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -925,8 +977,8 @@ int decode_max_parts(int max_blocks_per_seq) {
 
 size_t decode_workspace_bytes(int num_seqs, int Hq, int d, int max_blocks_per_seq) {
   // Partial O (d floats), max and sum per (sequence, query head, part), then
-  // the part count of every (sequence, KV head) (8 bytes per sequence and
-  // query head are reserved for it).
+  // the arrival counter of every (sequence, KV head) (8 bytes per sequence
+  // and query head are reserved for these).
   const size_t parts = static_cast<size_t>(num_seqs) * Hq * decode_max_parts(max_blocks_per_seq);
   return parts * (static_cast<size_t>(d) + 2) * sizeof(float) +
          static_cast<size_t>(num_seqs) * Hq * sizeof(unsigned long long);

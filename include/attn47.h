@@ -186,14 +186,21 @@ size_t attn_decode_paged_workspace_size(int num_seqs, int Hq, int d, int max_blo
  *  o            [num_seqs, Hq, d] bf16 (written)
  *  lse          [num_seqs, Hq] fp32 (written) or NULL
  *  workspace    >= attn_decode_paged_workspace_size(...) bytes, 16-byte
- *               aligned; contents on entry are ignored
+ *               aligned; contents on entry are ignored (the per-sequence
+ *               arrival counters in it carry a tag that differs on every
+ *               call, and each call leaves them at zero)
  *  block_size must be 16; d must be 64 or 128; Hq % Hkv == 0 and
  *  Hq / Hkv <= 16; num_blocks * Hkv * 16 < 2^31.
  *  num_seqs == 0 is an empty problem: returns ATTN_OK, launches nothing.
- *  Launches two kernels: the decode over an even split of all cached tokens
- *  (one CTA per SM), then the merge, in a fixed order, of the parts of
- *  sequences split across CTAs.  Calls that share a workspace must not
- *  overlap on the GPU.  Deterministic for a given device and
+ *  Launches one kernel over an even split of all cached tokens (one CTA per
+ *  SM); the parts of a (sequence, KV head) split across CTAs are merged
+ *  exactly by whichever part finishes last.  The kernel is launched as a
+ *  programmatic dependent of the preceding work in the stream: its CTAs may
+ *  start while that kernel drains and wait for it to finish before reading
+ *  q or the cache and before writing anything (see
+ *  attn_set_decode_early_plan for the one exception).  Calls that share a
+ *  workspace must not overlap on the GPU.  The result does not depend on
+ *  which part finishes last; it is deterministic for a given device and
  *  attn_set_decode_max_ctas setting.
  */
 attn_status_t attn_decode_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -410,6 +417,21 @@ void attn_set_wait_timeout_ns(unsigned long long ns);
  * process.
  */
 void attn_set_decode_max_ctas(int ctas);
+
+/*
+ * attn_set_decode_early_plan — 1: later decode calls (both entry points)
+ * read seq_lens and the first block-table entries of each CTA's share
+ * before the kernel that precedes them in the stream has finished, so that
+ * the split plan overlaps that kernel's tail; 0 (the default): they read
+ * nothing before it has finished.  With 1 the caller guarantees that
+ * seq_lens and block_table are not written by the kernel launched just
+ * before the decode on its stream (nor, if that kernel was itself launched
+ * as a programmatic dependent, by the one before it): write them with a
+ * host-to-device copy or an earlier kernel.  q and the cache may always be
+ * written by the preceding kernel.  Applies to later calls from this
+ * process.
+ */
+void attn_set_decode_early_plan(int on);
 
 /*
  * attn_selftest_exp2_poly — y[i] = 2^x[i] by an exp2 on the FMA pipe

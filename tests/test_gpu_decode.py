@@ -178,3 +178,113 @@ def test_bounded_wait_times_out_and_reports():
     x = torch.ones(4, device=DEV)
     assert float(x.sum()) == 4.0
     assert attn.device_status() == 0
+
+
+def _call(d, scale, o, lse, ws):
+    attn.attn_decode_paged(d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["seq_lens"],
+                           scale=scale, o=o, lse=lse, workspace=ws)
+
+
+def _outs(inp):
+    S, Hq, d = inp["q"].shape
+    return (torch.empty(S, Hq, d, dtype=torch.bfloat16, device=DEV),
+            torch.empty(S, Hq, dtype=torch.float32, device=DEV))
+
+
+def test_workspace_garbage_and_reuse():
+    """The per-run arrival counters live in the caller's workspace: random
+    bytes on entry, or the state another call left, must not change a
+    result.  Several CTAs per sequence, so most runs are split."""
+    a = workloads.decode_inputs(9, 12, 2, 128, seed=28, len_lo=1, len_hi=3000)
+    b = workloads.decode_inputs(5, 12, 2, 128, seed=29, seq_lens=[2990, 1, 600, 2048, 77], len_hi=3000)
+    mb = max(a["block_table"].shape[1], b["block_table"].shape[1])
+    need = attn.attn_decode_paged_workspace_size(9, 12, 128, mb)
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, generator=torch.Generator().manual_seed(3)).to(DEV)
+    da, db = to_dev(a), to_dev(b)
+    oa, la = _outs(a)
+    ob, lb = _outs(b)
+    try:
+        attn.set_decode_max_ctas(13)
+        _call(da, 0.1, oa, la, ws)
+        torch.cuda.synchronize()
+        first = (oa.clone(), la.clone())
+        _call(db, 0.1, ob, lb, ws)
+        _call(da, 0.1, oa, la, ws)
+        torch.cuda.synchronize()
+    finally:
+        attn.set_decode_max_ctas(0)
+    assert attn.device_status() == 0
+    assert_attn_close(first[0], first[1], *ref(a, 0.1), what="garbage workspace")
+    assert_attn_close(ob, lb, *ref(b, 0.1), what="reused workspace")
+    assert torch.equal(first[0], oa) and torch.equal(first[1], la)
+
+
+@pytest.mark.parametrize("early", [0, 1])
+def test_graph_replay_reuses_counters(early):
+    """A captured decode replays with the same counter tag every time; each
+    call must leave the counters as it found them.  Two decodes back to back
+    in one graph also exercise the programmatic dependency between them."""
+    a = workloads.decode_inputs(9, 12, 2, 128, seed=30, len_lo=1, len_hi=2500)
+    b = workloads.decode_inputs(9, 12, 2, 128, seed=31, len_lo=1, len_hi=2500)
+    da, db = to_dev(a), to_dev(b)
+    mb = max(a["block_table"].shape[1], b["block_table"].shape[1])
+    ws = torch.zeros(attn.attn_decode_paged_workspace_size(9, 12, 128, mb), dtype=torch.uint8, device=DEV)
+    oa, la = _outs(a)
+    ob, lb = _outs(b)
+    try:
+        attn.set_decode_early_plan(early)
+        _call(da, 0.1, oa, la, ws)
+        _call(db, 0.1, ob, lb, ws)
+        torch.cuda.synchronize()
+        eager = [t.clone() for t in (oa, la, ob, lb)]
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g):
+                _call(da, 0.1, oa, la, ws)
+                _call(db, 0.1, ob, lb, ws)
+        torch.cuda.current_stream().wait_stream(side)
+        for _ in range(3):
+            for t in (oa, la, ob, lb):
+                t.fill_(7.0)
+            g.replay()
+            torch.cuda.synchronize()
+            assert all(torch.equal(x, y) for x, y in zip(eager, (oa, la, ob, lb)))
+    finally:
+        attn.set_decode_early_plan(0)
+    assert attn.device_status() == 0
+    assert_attn_close(oa, la, *ref(a, 0.1), what="graph replay a")
+    assert_attn_close(ob, lb, *ref(b, 0.1), what="graph replay b")
+
+
+def test_early_plan_gives_identical_bits():
+    """The early plan only moves the split plan before the wait for the
+    preceding kernel: same split, same bits.  Chained calls with different
+    lengths check that no call plans with another's lengths."""
+    c = workloads.DECODE_CONFIGS["paged_decode"]
+    inps = [workloads.decode_inputs(c["num_seqs"], c["Hq"], c["Hkv"], c["d"], c["seed"] + 50 * i,
+                                    c["len_lo"], c["len_hi"]) for i in range(3)]
+    devs = [to_dev(x) for x in inps]
+    scale = workloads.default_scale(c["d"])
+    res = {}
+    for early in (0, 1):
+        try:
+            attn.set_decode_early_plan(early)
+            outs = []
+            for d in devs:
+                S = d["q"].shape[0]
+                mb = d["block_table"].shape[1]
+                ws = torch.empty(attn.attn_decode_paged_workspace_size(S, c["Hq"], c["d"], mb),
+                                 dtype=torch.uint8, device=DEV)
+                o, lse = _outs(d)
+                _call(d, scale, o, lse, ws)
+                outs.append((o, lse))
+            torch.cuda.synchronize()
+            res[early] = outs
+        finally:
+            attn.set_decode_early_plan(0)
+    assert attn.device_status() == 0
+    for (o0, l0), (o1, l1) in zip(res[0], res[1]):
+        assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert_attn_close(*res[1][2], *ref(inps[2], scale), what="early plan, third call")
