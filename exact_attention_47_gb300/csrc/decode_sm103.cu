@@ -66,12 +66,14 @@ constexpr float kTau = 8.f;
 constexpr int kQSlots = 8;
 constexpr int kMinChunk = 2 * kMinSplitBlocks;   // block-heads per CTA, lower bound
 // A CTA pays about this many blocks' worth of time for a (sequence, KV
-// head) run (query rows, the merge of the warp states, the output write, and
-// the warps' uneven finish at the run's end), so work is split by cost =
-// blocks + kRunCost per run, not by blocks alone.  Measured: 3, 6, 10 and 15
-// gave 37.5, 37.0, 37.3 and 36.8 us on 64 sequences of U[128, 4096] tokens
-// and 51.0, 48.6, 47.3 and 46.2 us on 256 of U[32, 1024].
-constexpr int kRunCost = 15;
+// head) run (query rows, the merge of the warp states, the output write or
+// the publication and merge of a split run's parts, and the warps' uneven
+// finish at the run's end), so work is split by cost = blocks + kRunCost per
+// run, not by blocks alone.  Measured (back-to-back calls on GB300, us per
+// call on 64 sequences of U[128, 4096] / 8 of 16384 / 256 of U[32, 1024]
+// tokens): 8: 31.5 / 32.6 / 37.4; 15: 29.6 / 32.7 / 35.8; 25: 29.3 / 32.8 /
+// 34.2; 40: 29.8 / 32.1 / 34.1.
+constexpr int kRunCost = 25;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Shared-memory layout for head dim D and groups of at most GM query heads
