@@ -68,9 +68,9 @@ TRAFFIC = {
     # median read + median write of 3 launches
     "fwd": {"bytes": 67206400 + 5443840, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
             "sha256": "644d0ed526136e30fd1a072177aa5d3e1af87c7ec15dc54c11a86248f6a9f82f"},
-    # decode kernel (split parts merged inside it), median of 3 launches
-    "dec": {"bytes": None, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
-            "sha256": None},
+    # decode kernel (split parts merged inside it), median read + median write of 3 launches
+    "dec": {"bytes": 132365312 + 144896, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
+            "sha256": "fa7e80560a69c522f5b0ec9e7ede8ca6b21068e844391bfea31a3ec9f973e1b7"},
 }
 
 
