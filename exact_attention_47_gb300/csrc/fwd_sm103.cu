@@ -228,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  // Launched as a programmatic dependent: the set-up above overlaps the end
+  // of the kernel before this one in the stream; nothing in global memory
+  // is read or written before that kernel has finished.
+  pdl_wait_primary();
   if constexpr (SORTED) {
     {
       // Cost key of pair (b, qblk): ctx_b + 256 * qblk (the K/V tiles of the
@@ -315,6 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv_issued += u.nB;
         ++units;
       }
+      // Every load is issued: the next kernel in the stream may start
+      // setting up on SMs this grid leaves (it waits for this grid to
+      // finish before it touches memory).
+      pdl_launch_dependents();
       // Every copy issued must have landed before the CTA may exit.
       if (units > 0)
         for (int x = 0; x < kTiles; ++x) mbar_wait(smem_addr(&bar->q_full[x]), (units - 1) & 1, wc, true);
@@ -774,8 +782,18 @@ cudaError_t launch_t(const FwdLaunch& a) {
   p.max_ctx = PAGED ? a.max_blocks * kPageRows - a.N : 0;
   // Persistent: one CTA per SM (shared memory allows one), each walking units.
   const unsigned grid = static_cast<unsigned>(min(p.num_units, a.sms > 0 ? a.sms : 1));
-  kern<<<grid, kThreads, L::kSmem, a.stream>>>(*a.tq, *a.tk, *a.tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, *a.tq, *a.tk, *a.tv, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
