@@ -88,6 +88,11 @@ __global__ void __launch_bounds__(256) attn_bwd_rowdot_kernel(const BwdParams p)
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
   for (long long r = static_cast<long long>(blockIdx.x) * warps + (threadIdx.x >> 5); r < rows;
        r += static_cast<long long>(gridDim.x) * warps) {
     const int bh = static_cast<int>(r / p.n_pad);
@@ -160,6 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
   constexpr uint32_t kColDQ = 256;
 
   if (warp == kWarpLoad) {
@@ -384,6 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem_base;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
   constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 
   if (warp == kWarpLoad) {
@@ -605,22 +620,21 @@ cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
   {
     const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
     const long long blocks = (rows + 7) / 8;
-    attn_bwd_rowdot_kernel<D><<<static_cast<unsigned>(min(blocks, 65535LL * 16)), 256, 0, a.stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(attn_bwd_rowdot_kernel<D>, dim3(static_cast<unsigned>(min(blocks, 65535LL * 16))),
+                                     dim3(256), 0, a.stream, p);
     if (e != cudaSuccess) return e;
   }
   auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  kq<<<static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_q), kThreads, L::kSmem, a.stream>>>(
-      *a.tq, *a.tk, *a.tv, *a.tdo, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(kq, dim3(static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_q)), dim3(kThreads), L::kSmem,
+                 a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
+  if (e != cudaSuccess) return e;
   auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
   e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  kkv<<<static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv), kThreads, L::kSmem, a.stream>>>(
-      *a.tq, *a.tk, *a.tv, *a.tdo, p);
-  return cudaGetLastError();
+  return launch_pdl(kkv, dim3(static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv)), dim3(kThreads),
+                    L::kSmem, a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
 }
 
 }  // namespace

@@ -16,6 +16,11 @@
 // stores, from L1/L2) and the weight and writes bf16(r * rsqrt(ms + eps) * w).
 // SwiGLU: grid-stride over 16-byte pieces of the output; gate and up pieces
 // of a row are F columns apart in the merged projection output.
+// Both are launched as programmatic dependents of the preceding kernel: they
+// wait for it (griddepcontrol.wait) before their first load, and let the
+// next kernel launch as soon as every CTA of theirs is running (measured:
+// a trigger after the loop made back-to-back SwiGLU calls 9 % slower than
+// no programmatic launch at all; this placement is 1.4 % faster).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,6 +43,8 @@ __global__ void __launch_bounds__(kNormThreads)
                        int pieces, float eps, float inv_hidden) {
   const int lane = threadIdx.x & 31;
   const int warps = static_cast<int>(gridDim.x) * (kNormThreads / 32);
+  pdl_wait_primary();
+  pdl_launch_dependents();
   for (int row = static_cast<int>(blockIdx.x) * (kNormThreads / 32) + (threadIdx.x >> 5); row < rows;
        row += warps) {
     const size_t base = static_cast<size_t>(row) * pieces;
@@ -94,6 +101,8 @@ __global__ void __launch_bounds__(kGluThreads)
     swiglu_kernel(const uint4* __restrict__ gate_up, uint4* __restrict__ out, long long total,
                   int fpieces) {
   const long long stride = static_cast<long long>(gridDim.x) * kGluThreads;
+  pdl_wait_primary();
+  pdl_launch_dependents();
   for (long long i = static_cast<long long>(blockIdx.x) * kGluThreads + threadIdx.x; i < total;
        i += stride) {
     const long long row = i / fpieces;
@@ -120,11 +129,10 @@ cudaError_t launch_add_rmsnorm_sm103(const NormLaunch& a) {
   const long long blocks = (static_cast<long long>(a.rows) + rows_per_block - 1) / rows_per_block;
   const long long cap = static_cast<long long>(a.sms > 0 ? a.sms : 1) * 8;   // 8 blocks (64 warps) per SM
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  add_rmsnorm_kernel<<<grid, kNormThreads, 0, a.stream>>>(
-      static_cast<const uint4*>(a.x), static_cast<uint4*>(a.residual),
-      static_cast<const uint4*>(a.weight), static_cast<uint4*>(a.out), a.rows, pieces, a.eps,
-      1.f / static_cast<float>(a.hidden));
-  return cudaGetLastError();
+  return launch_pdl(add_rmsnorm_kernel, dim3(grid), dim3(kNormThreads), 0, a.stream,
+                    static_cast<const uint4*>(a.x), static_cast<uint4*>(a.residual),
+                    static_cast<const uint4*>(a.weight), static_cast<uint4*>(a.out), a.rows, pieces, a.eps,
+                    1.f / static_cast<float>(a.hidden));
 }
 
 cudaError_t launch_swiglu_sm103(const GluLaunch& a) {
@@ -133,9 +141,8 @@ cudaError_t launch_swiglu_sm103(const GluLaunch& a) {
   const long long blocks = (total + kGluThreads - 1) / kGluThreads;
   const long long cap = static_cast<long long>(a.sms > 0 ? a.sms : 1) * 16;
   const unsigned grid = static_cast<unsigned>(blocks < cap ? blocks : cap);
-  swiglu_kernel<<<grid, kGluThreads, 0, a.stream>>>(static_cast<const uint4*>(a.gate_up),
-                                                    static_cast<uint4*>(a.out), total, fpieces);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_kernel, dim3(grid), dim3(kGluThreads), 0, a.stream,
+                    static_cast<const uint4*>(a.gate_up), static_cast<uint4*>(a.out), total, fpieces);
 }
 
 }  // namespace attn47

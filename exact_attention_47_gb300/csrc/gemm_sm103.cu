@@ -91,6 +91,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
 
   // Tiles of this CTA: blockIdx.x, + gridDim.x, ...; the row block varies
   // fastest, so the CTAs working at the same time share W tiles in L2.
@@ -222,8 +227,7 @@ cudaError_t launch_swiglu_proj_sm103(const SwigluProjLaunch& a) {
   cudaError_t e = cudaFuncSetAttribute(swiglu_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const int grid = p.tiles < a.sms ? p.tiles : a.sms;
-  swiglu_proj_kernel<<<grid, kThreads, kSmem, a.stream>>>(*a.tx, *a.tw, p);
-  return cudaGetLastError();
+  return launch_pdl(swiglu_proj_kernel, dim3(grid), dim3(kThreads), kSmem, a.stream, *a.tx, *a.tw, p);
 }
 
 }  // namespace attn47

@@ -153,6 +153,11 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -506,6 +511,11 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = bar->tmem;
   const WaitCtl wc{&bar->abort, p.status, p.timeout_ns};
+  // Programmatic dependent launch: nothing global is touched before the
+  // preceding kernel has finished; the next kernel may start its set-up as
+  // soon as every CTA of this grid is running.
+  pdl_wait_primary();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -768,13 +778,12 @@ cudaError_t launch_nq(const SsdLaunch& a, const SsdParams& p) {
   if (e != cudaSuccess) return e;
   const int hpg = a.H / a.G;
   const long long grid1 = static_cast<long long>(a.batch) * a.G * ((hpg + 1) / 2);
-  ks<<<static_cast<unsigned>(grid1), 192, Ls::kSmem, a.stream>>>(*a.tx, *a.tb, p);
-  e = cudaGetLastError();
+  e = launch_pdl(ks, dim3(static_cast<unsigned>(grid1)), dim3(192), Ls::kSmem, a.stream, *a.tx, *a.tb, p);
   if (e != cudaSuccess) return e;
   const long long grid2 = static_cast<long long>(a.batch) * p.nc * ((Q + 127) / 128) * a.G *
                           ((hpg + kHeadsPerOut - 1) / kHeadsPerOut);
-  ko<<<static_cast<unsigned>(grid2), 320, kOutSmem, a.stream>>>(*a.tx, *a.tb, *a.tc, *a.ts, p);
-  return cudaGetLastError();
+  return launch_pdl(ko, dim3(static_cast<unsigned>(grid2)), dim3(320), kOutSmem, a.stream, *a.tx, *a.tb, *a.tc,
+                    *a.ts, p);
 }
 
 }  // namespace
