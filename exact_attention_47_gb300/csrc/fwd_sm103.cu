@@ -688,22 +688,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // The stabiliser only has to keep the numerators finite (fp32 and
+      // bf16 reach 2^127), so after the first tile the tile's maximum is not
+      // formed up front: the numerators are computed with the current m, and
+      // only a tile whose fp32 sum exceeds 2^100 (or is not finite) is redone
+      // with the stabiliser moved to its maximum.  Same function, same
+      // rounding.  One call site, so the unrolled loop is emitted once.
       if (j == 0) {
         const float mt = row_max() * sl2;
         m = (mt == -INFINITY) ? 0.f : mt;
+      }
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
         numerators();
-      } else {
-        // The stabiliser only has to keep the numerators finite (fp32 and
-        // bf16 reach 2^127), so the tile's maximum is not formed up front:
-        // the numerators are computed with the current m, and only a tile
-        // whose fp32 sum exceeds 2^100 (or is not finite) is redone with the
-        // stabiliser moved to its maximum.  Same function, same rounding.
-        numerators();
+        if (j == 0 || pass == 1) break;
         const bool big = !(lt <= 0x1p100f);
-        if (__any_sync(0xffffffffu, big)) {
-          restabilise();
-          numerators();
-        }
+        if (!__any_sync(0xffffffffu, big)) break;
+        restabilise();
       }
       l += lt;
       lr += lrt;
