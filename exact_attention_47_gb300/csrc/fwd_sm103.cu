@@ -661,8 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Moves the stabiliser to the tile's maximum where that exceeds it by
       // more than kTau, rescaling the sums and O_X (which holds PV_X(0..j-1),
       // complete since S_X(j) completed after it).
-      auto restabilise = [&]() {
-        const float mt = row_max() * sl2;
+      auto restabilise = [&](float mt) {
         const bool need = mt > m + kTau;
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = need ? mt : m;
@@ -694,17 +693,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // only a tile whose fp32 sum exceeds 2^100 (or is not finite) is redone
       // with the stabiliser moved to its maximum.  Same function, same
       // rounding.  One call site, so the unrolled loop is emitted once.
-      if (j == 0) {
-        const float mt = row_max() * sl2;
-        m = (mt == -INFINITY) ? 0.f : mt;
-      }
 #pragma unroll 1
       for (int pass = 0; pass < 2; ++pass) {
+        if (j == 0 || pass == 1) {                 // the tile's maximum is needed
+          const float mt = row_max() * sl2;
+          if (j == 0)
+            m = (mt == -INFINITY) ? 0.f : mt;
+          else
+            restabilise(mt);
+        }
         numerators();
         if (j == 0 || pass == 1) break;
         const bool big = !(lt <= 0x1p100f);
         if (!__any_sync(0xffffffffu, big)) break;
-        restabilise();
       }
       l += lt;
       lr += lrt;
