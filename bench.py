@@ -24,7 +24,10 @@ to back over the three rotated KV pools; the decode's time inside the step,
 where it follows the forward's still-dirty output in L2, is reported beside
 it), rooflines
 against the measured peaks, the same metric end to end through the public
-API with pinned host buffers ("e2e"), the fp64 oracle on host cores
+API with pinned host buffers ("e2e": every step uploads its inputs and reads
+its results back; steps are pipelined over the three device sets with the
+copies on two copy streams beside the compute stream, and the one-stream
+figure is reported beside it), the fp64 oracle on host cores
 ("cpu_baseline"), and the SM clocks sampled while the GPU ran.
 
 L2: three input sets (about 0.75 GB in total, above the 129 MB L2) are used
@@ -653,38 +656,86 @@ def run_gpu(args, rank, world, local_rank):
     h_q, h_k, h_v = (host[x].pin_memory() for x in ("q", "k", "v"))
     hd = host["dec"]
     h_dq, h_bt, h_sl = hd["q"].pin_memory(), hd["block_table"].pin_memory(), hd["seq_lens"].pin_memory()
-    h_o = torch.empty(h_q.shape, dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty(h_q.shape[:3], dtype=torch.float32).pin_memory()
-    h_do = torch.empty(h_dq.shape, dtype=torch.bfloat16).pin_memory()
-    h_dlse = torch.empty(h_dq.shape[:2], dtype=torch.float32).pin_memory()
+    # One set of pinned result buffers per device input set, so the read-backs
+    # of consecutive steps never share a host buffer.
+    h_out = [dict(o=torch.empty(h_q.shape, dtype=torch.bfloat16).pin_memory(),
+                  lse=torch.empty(h_q.shape[:3], dtype=torch.float32).pin_memory(),
+                  do=torch.empty(h_dq.shape, dtype=torch.bfloat16).pin_memory(),
+                  dlse=torch.empty(h_dq.shape[:2], dtype=torch.float32).pin_memory()) for _ in range(NSETS)]
     h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_dq, h_bt, h_sl))
-    d2h = sum(t.numel() * t.element_size() for t in (h_o, h_lse, h_do, h_dlse))
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
 
-    def e2e_step(s):
+    def upload(s):
         s["q"].copy_(h_q, non_blocking=True)
         s["k"].copy_(h_k, non_blocking=True)
         s["v"].copy_(h_v, non_blocking=True)
         s["dq"].copy_(h_dq, non_blocking=True)
         s["bt"].copy_(h_bt, non_blocking=True)
         s["sl"].copy_(h_sl, non_blocking=True)
+
+    def download(s, ho):
+        ho["o"].copy_(s["o"], non_blocking=True)
+        ho["lse"].copy_(s["lse"], non_blocking=True)
+        ho["do"].copy_(s["do"], non_blocking=True)
+        ho["dlse"].copy_(s["dlse"], non_blocking=True)
+
+    def e2e_serial_step(i):
+        s = sets[i % NSETS]
+        upload(s)
         fwd(s)
         dec(s)
-        h_o.copy_(s["o"], non_blocking=True)
-        h_lse.copy_(s["lse"], non_blocking=True)
-        h_do.copy_(s["do"], non_blocking=True)
-        h_dlse.copy_(s["dlse"], non_blocking=True)
+        download(s, h_out[i % NSETS])
+
+    # Pipelined: step i's uploads run on one copy stream while the kernels of
+    # step i - 1 run, and its read-backs on another; a device set is uploaded
+    # again only once the read-back of the step that last used it is done.
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    set_free = [None] * NSETS
+
+    def e2e_step(i):
+        j = i % NSETS
+        s = sets[j]
+        if set_free[j] is not None:
+            up.wait_event(set_free[j])
+        with torch.cuda.stream(up):
+            upload(s)
+        inputs_in = torch.cuda.Event()
+        inputs_in.record(up)
+        stream.wait_event(inputs_in)
+        fwd(s)
+        dec(s)
+        results = torch.cuda.Event()
+        results.record(stream)
+        down.wait_event(results)
+        with torch.cuda.stream(down):
+            download(s, h_out[j])
+        set_free[j] = torch.cuda.Event()
+        set_free[j].record(down)
+
+    def timed_e2e(step, n):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        up.wait_event(e0)
+        down.wait_event(e0)
+        for i in range(n):
+            step(i)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
 
     for i in range(max(1, min(args.warmup, 3))):
-        e2e_step(sets[i % NSETS])
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(K):
-        e2e_step(sets[i % NSETS])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
+        e2e_step(i)
+    e2e_ms = timed_e2e(e2e_step, K)
+    # Every step's read-back is complete: the last step's results equal the
+    # device outputs they were copied from.
+    last = (K - 1) % NSETS
+    e2e_ok = bool(torch.equal(h_out[last]["o"], sets[last]["o"].cpu()) and
+                  torch.equal(h_out[last]["dlse"], sets[last]["dlse"].cpu()))
+    e2e_serial_ms = timed_e2e(e2e_serial_step, max(50, K // 10))
     clock.stop()
     pk_all, _ = peaks()
     side = max(10, min(K, 200))      # calls per measurement outside the step
@@ -696,8 +747,8 @@ def run_gpu(args, rank, world, local_rank):
     ssd = ssd_measurement(attn, device, side, pk_all["bf16_tflops"], pk_all["hbm_gbs"])
 
     # ---- max over ranks
-    total_ms, fwd_sum, dec_sum, e2e_ms, dec_alone_ms = max_over_ranks(
-        [total_ms, sum(fwd_ms), sum(dec_ms), e2e_ms, dec_alone_ms], dist, device)
+    total_ms, fwd_sum, dec_sum, e2e_ms, dec_alone_ms, e2e_serial_ms = max_over_ranks(
+        [total_ms, sum(fwd_ms), sum(dec_ms), e2e_ms, dec_alone_ms, e2e_serial_ms], dist, device)
 
     if rank == 0:
         pk, pk_kind = peaks()
@@ -748,7 +799,13 @@ def run_gpu(args, rank, world, local_rank):
             "e2e": {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "note": "fwd flops over the whole step: pinned h2d of q,k,v and of the "
-                            "decode query/table/lengths, both ops, d2h of all outputs"},
+                            "decode query/table/lengths, both ops, d2h of all outputs; steps "
+                            "pipelined over the 3 device sets (uploads and read-backs on two copy "
+                            "streams beside the compute stream)",
+                    "readback_matches_device": e2e_ok,
+                    "serial": {"value": world * flops / (e2e_serial_ms / 1e3) / 1e12,
+                               "ms_per_step": e2e_serial_ms,
+                               "note": "the same step with copies and kernels in one stream"}},
             "fwd_configs": dict(fwd_configs, **{FWD_CFG: {
                 "shape": "B4 Hq12 Hkv2 N4096 d128 causal", "ms": fwd_sum / K,
                 "tflops": achieved_fwd, "frac": achieved_fwd / pk["bf16_tflops"]}}),
