@@ -18,15 +18,16 @@
 //               entries a batch of 32 blocks ahead; per segment bulk-copies
 //               the G query rows; per block TMA-copies the (block, head) K
 //               and V slices (16 x d bf16, 128-byte swizzle; one copy each)
-//               into a ring of 21 stages (14 when G > 8)
+//               into a ring of 21 stages (14 when G > 8), with an
+//               evict-first L2 policy (every cached byte is read once)
 //   warps 0..6  consumers: block c of the chunk goes to warp c % 7, which
 //               moves its K and V fragments to registers and hands the stage
 //               back before computing; scores and P V are 16x8x16 warp MMAs
 //               (rows = the G query heads, zero-padded to 16); at the
 //               segment's end the seven warp states are merged in shared
 //               memory
-// A segment that covers a whole sequence writes O and LSE directly; the
-// others publish an unnormalised partial (O, max, sum) and count their
+// A segment that covers a whole (sequence, KV head) run writes O and LSE
+// directly; the others publish an unnormalised partial (O, max, sum) and count their
 // arrival on the run's counter; the part that arrives last merges all parts
 // of the run (exactly, with their maxima) and writes O and LSE.
 //

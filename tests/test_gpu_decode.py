@@ -288,3 +288,13 @@ def test_early_plan_gives_identical_bits():
     for (o0, l0), (o1, l1) in zip(res[0], res[1]):
         assert torch.equal(o0, o1) and torch.equal(l0, l1)
     assert_attn_close(*res[1][2], *ref(inps[2], scale), what="early plan, third call")
+
+
+def test_long_sequences_split_into_many_parts():
+    """Eight 16384-token sequences over one wave: every (sequence, KV head)
+    run is split over about ten CTAs, so the part that arrives last merges
+    ten or more published parts (several passes of the merge)."""
+    inp = workloads.decode_inputs(8, 12, 2, 128, seed=32, len_lo=16384, len_hi=16384)
+    o, lse = run(inp, 0.088)
+    assert attn.device_status() == 0
+    assert_attn_close(o, lse, *ref(inp, 0.088), what="8 x 16384 tokens")
