@@ -72,8 +72,8 @@ TRAFFIC = {
     "fwd": {"bytes": 67193856 + 5175296, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
             "sha256": "b79a891c57339e93b10115318d450c7ffbbfa694aaa58f0473fdfbc1cab5a63a"},
     # decode kernel (split parts merged inside it), median read + median write of 3 launches
-    "dec": {"bytes": 132369152 + 481280, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
-            "sha256": "75c05cbc2c931656390bc95939c51afadffae098a8ba915f70b4da9ac644fa06"},
+    "dec": {"bytes": 132367360 + 156416, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
+            "sha256": "187f4e34dc366543f8a3ee8b14ca508bde250f0635a7db971bf7984c3debc55d"},
 }
 
 
