@@ -83,35 +83,66 @@ static_assert(sizeof(BwdBarriers) <= 256, "barrier block");
 // ------------------------------------------------------------------ row dot
 // D[r] = sum_c dO[r, c] * O[r, c] and lse2[r] = lse[r] * log2(e) for the
 // query rows of every (batch, head), rows padded to whole tiles with zeros.
+// A row is D / 8 sixteen-byte pieces, one per lane, so one load instruction
+// of a warp covers 32 / (D / 8) rows; a warp takes kRowDotPasses such groups
+// of consecutive rows and has all their loads in flight before it reduces.
+constexpr int kRowDotPasses = 4;
+
+template <int D>
+__host__ __device__ constexpr int rowdot_rows_per_warp() { return 32 / (D / 8) * kRowDotPasses; }
+
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_rowdot_kernel(const BwdParams p) {
-  const int warps = blockDim.x >> 5;
+  constexpr int kPieces = D / 8;                   // lanes per row
+  constexpr int kRowsPerPass = 32 / kPieces;
   const int lane = threadIdx.x & 31;
+  const int piece = lane % kPieces;
+  const int sub = lane / kPieces;
   const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   // Programmatic dependent launch: nothing global is touched before the
   // preceding kernel has finished; the next kernel may start its set-up as
   // soon as every CTA of this grid is running.
   pdl_wait_primary();
   pdl_launch_dependents();
-  for (long long r = static_cast<long long>(blockIdx.x) * warps + (threadIdx.x >> 5); r < rows;
-       r += static_cast<long long>(gridDim.x) * warps) {
-    const int bh = static_cast<int>(r / p.n_pad);
-    const int n = static_cast<int>(r % p.n_pad);
-    float dsum = 0.f, lse2 = 0.f;
-    if (n < p.N) {
-      const size_t base = (static_cast<size_t>(bh) * p.N + n) * D;
-      constexpr int kPer = D / 32;                 // bf16 elements per lane (2 or 4)
-      const __nv_bfloat16* po = p.o + base + lane * kPer;
-      const __nv_bfloat16* pd = p.dout + base + lane * kPer;
+  for (long long r0 = (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) *
+                      rowdot_rows_per_warp<D>();
+       r0 < rows; r0 += warps * rowdot_rows_per_warp<D>()) {
+    uint4 ov[kRowDotPasses], dv[kRowDotPasses];
+    float lse[kRowDotPasses];
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) dsum += __bfloat162float(po[e]) * __bfloat162float(pd[e]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-      lse2 = p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e;
+    for (int i = 0; i < kRowDotPasses; ++i) {
+      const long long r = r0 + i * kRowsPerPass + sub;
+      const long long bh = r / p.n_pad;
+      const int n = static_cast<int>(r - bh * p.n_pad);
+      ov[i] = dv[i] = make_uint4(0u, 0u, 0u, 0u);
+      lse[i] = 0.f;
+      if (r < rows && n < p.N) {
+        const size_t row = static_cast<size_t>(bh) * p.N + n;
+        ov[i] = __ldg(reinterpret_cast<const uint4*>(p.o + row * D) + piece);
+        dv[i] = __ldg(reinterpret_cast<const uint4*>(p.dout + row * D) + piece);
+        if (piece == 0) lse[i] = p.lse[row] * kLog2e;
+      }
     }
-    if (lane == 0) {
-      p.ws_d[r] = dsum;
-      p.ws_lse2[r] = lse2;
+#pragma unroll
+    for (int i = 0; i < kRowDotPasses; ++i) {
+      const unsigned ow[4] = {ov[i].x, ov[i].y, ov[i].z, ov[i].w};
+      const unsigned dw[4] = {dv[i].x, dv[i].y, dv[i].z, dv[i].w};
+      float dsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ow[w]));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[w]));
+        dsum += a.x * b.x;
+        dsum += a.y * b.y;
+      }
+#pragma unroll
+      for (int o = kPieces / 2; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+      const long long r = r0 + i * kRowsPerPass + sub;
+      if (piece == 0 && r < rows) {
+        p.ws_d[r] = dsum;
+        p.ws_lse2[r] = lse[i];
+      }
     }
   }
 }
@@ -619,7 +650,8 @@ cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
   const int nq = (a.N + kTile - 1) / kTile;
   {
     const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
-    const long long blocks = (rows + 7) / 8;
+    const long long per_cta = 8LL * rowdot_rows_per_warp<D>();   // eight warps
+    const long long blocks = (rows + per_cta - 1) / per_cta;
     const cudaError_t e = launch_pdl(attn_bwd_rowdot_kernel<D>, dim3(static_cast<unsigned>(min(blocks, 65535LL * 16))),
                                      dim3(256), 0, a.stream, p);
     if (e != cudaSuccess) return e;
