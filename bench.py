@@ -397,7 +397,7 @@ def bwd_measurement(attn, device, steps, peak):
     tflops = 2.5 * fwd_flops(c) / (ms / 1e3) / 1e12
     return {"workload": FWD_CFG + " (B4 Hq12 Hkv2 N4096 d128 causal)", "ms": ms, "tflops": tflops,
             "frac": tflops / peak, "flop_convention": "2.5 x forward (5 matmuls vs 2)",
-            "kernels": "rowdot + dq + dkdv"}
+            "kernels": "rowdot + one grid of dK/dV and dQ tiles"}
 
 
 def paged_prefill_flops(ctx_lens, Hq, N, d):

@@ -10,12 +10,13 @@
 // The score matrix never reaches HBM; with GQA the K/V gradients of a KV
 // head are accumulated over its query heads inside one CTA.
 //
-// Three kernels, in stream order:
+// Two kernels, in stream order:
 //   attn_bwd_rowdot_kernel     D and lse * log2(e) per query row (HBM-bound)
-//   attn_bwd_dq_kernel         one 128-row query tile per CTA, loops over K/V
-//   attn_bwd_dkdv_kernel       one 128-key tile per CTA, loops over the query
-//                              tiles of every query head of its group
-// Both tile kernels: warps 0-7 compute (warp w: TMEM lanes 32 (w % 4) .., one
+//   attn_bwd_kernel            one tile per CTA, of one of two kinds:
+//     dK/dV: one 128-key tile, looping over the query tiles of every query
+//            head of its group;
+//     dQ:    one 128-row query tile, looping over K/V.
+// Both kinds of tile: warps 0-7 compute (warp w: TMEM lanes 32 (w % 4) .., one
 // row per thread, and columns 64 (w / 4) .. of the 128-wide score tiles; no
 // value crosses columns, since the LSE and D are precomputed), warp 8 the
 // TMA producer, warp 9 the MMA issuer and TMEM owner.  All contractions are
@@ -164,11 +165,10 @@ __device__ __forceinline__ void init_barriers(BwdBarriers* bar, int tid) {
 }
 
 // ------------------------------------------------------------------- dQ
+// Query tile `unit` of the dQ work (heaviest first under the causal mask).
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                       const BwdParams p) {
+__device__ __forceinline__ void bwd_dq_tile(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                            const CUtensorMap& tdo, const BwdParams& p, int unit) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int nq = (p.N + kTile - 1) / kTile;
-  const int qt = nq - 1 - static_cast<int>(blockIdx.x) / p.bh_q;   // heaviest (last) tiles first
-  const int bh = static_cast<int>(blockIdx.x) % p.bh_q;             // b * Hq + h
+  const int qt = nq - 1 - unit / p.bh_q;                            // heaviest (last) tiles first
+  const int bh = unit % p.bh_q;                                     // b * Hq + h
   const int zkv = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
   const int kv_total = nq;
   const int n_kv = CAUSAL ? min(qt + 1, kv_total) : kv_total;
@@ -386,11 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------- dK, dV
+// Key tile `unit` of the dK/dV work (heaviest first under the causal mask).
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                         const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                         const BwdParams p) {
+__device__ __forceinline__ void bwd_dkdv_tile(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                              const CUtensorMap& tdo, const BwdParams& p, int unit) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align1024(smem_raw);
@@ -404,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int nq = (p.N + kTile - 1) / kTile;
-  const int kt = static_cast<int>(blockIdx.x) / p.bh_kv;            // first key tiles see most queries
-  const int bhk = static_cast<int>(blockIdx.x) % p.bh_kv;           // b * Hkv + g
+  const int kt = unit / p.bh_kv;                                    // first key tiles see most queries
+  const int bhk = unit % p.bh_kv;                                   // b * Hkv + g
   const int b = bhk / p.Hkv, g = bhk % p.Hkv;
   const int qt0 = CAUSAL ? kt : 0;
   const int per_head = nq - qt0;
@@ -644,6 +643,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------------ one launch
+// The dK/dV and dQ work are independent (both read only the row-dot pass's
+// output), so one grid carries both: the dK/dV key tiles first (the largest
+// units: a key tile of a KV head covers the query tiles of all its query
+// heads), then the dQ query tiles, heaviest first.  The many small dQ units
+// fill the SMs that the dK/dV units' uneven causal sizes leave idle.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdParams p) {
+  const int n_kv_units = (p.N + kTile - 1) / kTile * p.bh_kv;
+  const int unit = static_cast<int>(blockIdx.x);
+  if (unit < n_kv_units) bwd_dkdv_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit);
+  else bwd_dq_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit - n_kv_units);
+}
+
 template <int D, bool CAUSAL>
 cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
   using L = BwdLayout<D>;
@@ -656,17 +672,11 @@ cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
                                      dim3(256), 0, a.stream, p);
     if (e != cudaSuccess) return e;
   }
-  auto kq = attn_bwd_dq_kernel<D, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  auto k = attn_bwd_kernel<D, CAUSAL>;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(kq, dim3(static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_q)), dim3(kThreads), L::kSmem,
-                 a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
-  if (e != cudaSuccess) return e;
-  auto kkv = attn_bwd_dkdv_kernel<D, CAUSAL>;
-  e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(kkv, dim3(static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv)), dim3(kThreads),
-                    L::kSmem, a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
+  const unsigned units = static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv + p.bh_q);
+  return launch_pdl(k, dim3(units), dim3(kThreads), L::kSmem, a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
 }
 
 }  // namespace
