@@ -420,10 +420,13 @@ def set_decode_max_ctas(ctas):
 
 
 def set_decode_early_plan(on):
-    """Let later decode calls read seq_lens and block_table before the
-    preceding kernel in the stream has finished (the caller guarantees that
-    kernel writes neither)."""
-    load_library().attn_set_decode_early_plan(1 if on else 0)
+    """Let later decode calls read seq_lens and block_table (``on`` = 1 or
+    True), and also the first cache blocks of each CTA's share except a
+    sequence's last block (``on`` = 2), before the preceding kernel in the
+    stream has finished; the caller guarantees that kernel writes none of
+    them.  0 or False: read nothing before it has finished."""
+    level = int(on)
+    load_library().attn_set_decode_early_plan(0 if level <= 0 else 2 if level >= 2 else 1)
 
 
 def selftest_exp2_poly(x, y=None, stream=None):

@@ -47,7 +47,7 @@ attn_status_t fail(attn_status_t s, const char* fmt, ...) {
 unsigned long long g_timeout_ns = 1000000000ull;
 
 int g_decode_max_ctas = 0;  // 0 = one full wave
-std::atomic<bool> g_decode_early_plan{false};
+std::atomic<int> g_decode_early_plan{0};
 
 // Tags of the decode's per-run arrival counters: a different nonzero value
 // for every call of this process, starting from a clock-derived value so
@@ -354,7 +354,7 @@ void attn_set_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns < 1000u
 
 void attn_set_decode_max_ctas(int ctas) { g_decode_max_ctas = ctas > 0 ? ctas : 0; }
 
-void attn_set_decode_early_plan(int on) { g_decode_early_plan.store(on != 0); }
+void attn_set_decode_early_plan(int on) { g_decode_early_plan.store(on <= 0 ? 0 : on >= 2 ? 2 : 1); }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int Hq, int Hkv, int N, int d, int causal, float scale, void* stream) {

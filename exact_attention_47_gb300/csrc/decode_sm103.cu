@@ -129,7 +129,8 @@ struct DecParams {
   unsigned long long* arrive;      // arrival counter per (sequence, KV head): tag << 32 | parts arrived
   int num_seqs, Hq, Hkv, group, max_blocks, num_blocks, max_parts;
   unsigned int epoch;              // this call's tag (never 0)
-  int early_plan;                  // plan before waiting for the preceding kernel
+  int early_plan;                  // 1: plan before waiting for the preceding kernel;
+                                   // 2: also stream the ring's first fill before it
   float scale_log2;
   unsigned int* status;
   unsigned long long timeout_ns;
@@ -612,16 +613,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       lw.skip(p, 32);
     };
     int cur_ph, cur_b, cur_g, n1_ph, n1_b, n1_g, n2_ph, n2_b, n2_g;
+    // Whether this lane's block of the first batch is the last block of its
+    // sequence (the one that holds the newest token).
+    const bool cur_last = lane < nblocks && lw.remaining > 0 && lw.blk == lw.nblk - 1;
     fetch(lane, cur_ph, cur_b, cur_g);
     fetch(32 + lane, n1_ph, n1_b, n1_g);
     fetch(64 + lane, n2_ph, n2_b, n2_g);
-    // Everything from here on may read what the preceding kernel wrote (the
-    // queries, the newest cache slots) or write what it reads.
-    pdl_wait_primary();
-
     // Every cached K/V byte is read once: keep it from evicting the
     // published parts and arrival counters that other CTAs read back.
     const uint64_t stream_policy = l2_policy_evict_first();
+    // Early stream: the ring's first fill (blocks 0 .. kStages-1 of the
+    // chunk, whose stages have never been used) is issued before the wait,
+    // except a sequence's last block and table entries outside the pool,
+    // which the loop below issues (or reports) after it.  Only K and V are
+    // read here; the query rows of the segments that start in these blocks
+    // are loaded after the wait.
+    unsigned pre = 0;
+    if (p.early_plan == 2) {
+      const bool early = lane < kStages && lane < nblocks && !cur_last && cur_ph >= 0 && cur_ph < p.num_blocks;
+      if (early) {
+        const uint32_t fb = smem_addr(&sh->full[lane]);
+        const int rowk = (cur_ph * p.Hkv + cur_g) * kBS;
+        const uint32_t dst = ring + lane * Lt::kStage;
+        sh->phys[lane] = cur_ph;
+        sh->fills[lane] = 1;
+        mbar_arrive_expect_tx(fb, Lt::kStage);
+        tma_load_3d_hint(dst, &tk, fb, 0, rowk, 0, stream_policy);
+        tma_load_3d_hint(dst + Lt::kHalf, &tv, fb, 0, rowk, 0, stream_policy);
+      }
+      pre = __ballot_sync(0xffffffffu, early);
+    }
+    // Everything from here on may read what the preceding kernel wrote (the
+    // queries, the newest cache slots) or write what it reads.
+    pdl_wait_primary();
     int seg = 0, carry_b = -1, carry_g = -1;
     bool ok = true;
     const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2;
@@ -658,8 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               sh->qfills[qs] = sego / kQSlots + 1;
             }
           }
-          if (okl) okl = mbar_wait(smem_addr(&sh->empty[st]), (fill & 1) ^ 1, wc);
-          if (okl) {
+          const bool issued = base == 0 && ((pre >> lane) & 1u);   // by the early stream
+          if (okl && !issued) okl = mbar_wait(smem_addr(&sh->empty[st]), (fill & 1) ^ 1, wc);
+          if (okl && !issued) {
             if (cur_ph < 0 || cur_ph >= p.num_blocks) {
               atomicOr(p.status, kDevBadBlock);    // outside the pool: that block is skipped
               cur_ph = -1;
@@ -947,7 +972,7 @@ cudaError_t launch_t(const DecLaunch& a) {
   p.num_blocks = a.num_blocks;
   p.max_parts = max_parts;
   p.epoch = a.epoch;
-  p.early_plan = a.early_plan ? 1 : 0;
+  p.early_plan = a.early_plan < 0 ? 0 : a.early_plan > 2 ? 2 : a.early_plan;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;

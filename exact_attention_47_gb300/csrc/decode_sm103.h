@@ -29,7 +29,8 @@ struct DecLaunch {
   int num_seqs, Hq, Hkv, d, max_blocks, num_blocks;
   int sms;                 // SM count of the device
   int max_ctas;            // 0: one full wave of CTAs
-  bool early_plan;         // read seq_lens / block_table before the preceding kernel ends
+  int early_plan;          // 1: read seq_lens / block_table before the preceding kernel ends;
+                           // 2: also the ring's first fill of cache blocks (not a sequence's last)
   unsigned int epoch;      // per-call tag of the arrival counters (never 0)
   float scale;
   unsigned int* status;

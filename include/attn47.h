@@ -422,14 +422,21 @@ void attn_set_decode_max_ctas(int ctas);
  * attn_set_decode_early_plan — 1: later decode calls (both entry points)
  * read seq_lens and the first block-table entries of each CTA's share
  * before the kernel that precedes them in the stream has finished, so that
- * the split plan overlaps that kernel's tail; 0 (the default): they read
- * nothing before it has finished.  With 1 the caller guarantees that
- * seq_lens and block_table are not written by the kernel launched just
- * before the decode on its stream (nor, if that kernel was itself launched
- * as a programmatic dependent, by the one before it): write them with a
- * host-to-device copy or an earlier kernel.  q and the cache may always be
- * written by the preceding kernel.  Applies to later calls from this
- * process.
+ * the split plan overlaps that kernel's tail; 2: as 1, and each CTA also
+ * starts streaming the first cache blocks of its share (up to its ring's
+ * depth, 21 blocks for up to 8 query heads per KV head, 14 above) before
+ * that kernel has finished, except the last block of each sequence (the
+ * block holding position seq_lens[b] - 1, where a decode step appends its
+ * newest token); 0 (the default): they read nothing before it has
+ * finished.  With 1 or 2 the caller guarantees that seq_lens and
+ * block_table — and with 2 every cache block other than each sequence's
+ * last — are not written by the kernel launched just before the decode on
+ * its stream (nor, if that kernel was itself launched as a programmatic
+ * dependent, by the one before it): write them with a host-to-device copy
+ * or an earlier kernel.  q and each sequence's last cache block may always
+ * be written by the preceding kernel.  Results are the same bits at every
+ * level.  Values above 2 act as 2, below 0 as 0.  Applies to later calls
+ * from this process.
  */
 void attn_set_decode_early_plan(int on);
 

@@ -219,7 +219,7 @@ def test_workspace_garbage_and_reuse():
     assert torch.equal(first[0], oa) and torch.equal(first[1], la)
 
 
-@pytest.mark.parametrize("early", [0, 1])
+@pytest.mark.parametrize("early", [0, 1, 2])
 def test_graph_replay_reuses_counters(early):
     """A captured decode replays with the same counter tag every time; each
     call must leave the counters as it found them.  Two decodes back to back
@@ -259,16 +259,17 @@ def test_graph_replay_reuses_counters(early):
 
 
 def test_early_plan_gives_identical_bits():
-    """The early plan only moves the split plan before the wait for the
-    preceding kernel: same split, same bits.  Chained calls with different
-    lengths check that no call plans with another's lengths."""
+    """The early plan only moves the split plan (level 1), and the first
+    cache copies (level 2), before the wait for the preceding kernel: same
+    split, same bits.  Chained calls with different lengths check that no
+    call plans with another's lengths."""
     c = workloads.DECODE_CONFIGS["paged_decode"]
     inps = [workloads.decode_inputs(c["num_seqs"], c["Hq"], c["Hkv"], c["d"], c["seed"] + 50 * i,
                                     c["len_lo"], c["len_hi"]) for i in range(3)]
     devs = [to_dev(x) for x in inps]
     scale = workloads.default_scale(c["d"])
     res = {}
-    for early in (0, 1):
+    for early in (0, 1, 2):
         try:
             attn.set_decode_early_plan(early)
             outs = []
@@ -285,9 +286,10 @@ def test_early_plan_gives_identical_bits():
         finally:
             attn.set_decode_early_plan(0)
     assert attn.device_status() == 0
-    for (o0, l0), (o1, l1) in zip(res[0], res[1]):
-        assert torch.equal(o0, o1) and torch.equal(l0, l1)
-    assert_attn_close(*res[1][2], *ref(inps[2], scale), what="early plan, third call")
+    for level in (1, 2):
+        for (o0, l0), (o1, l1) in zip(res[0], res[level]):
+            assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    assert_attn_close(*res[2][2], *ref(inps[2], scale), what="early plan, third call")
 
 
 def test_long_sequences_split_into_many_parts():

@@ -61,11 +61,12 @@ def test_forward_output_read_just_after():
     assert torch.equal(first, o_a.float().sum(dim=-1))
 
 
-@pytest.mark.parametrize("early", [0, 1])
+@pytest.mark.parametrize("early", [0, 1, 2])
 def test_decode_sees_lengths_and_queries_written_just_before(early):
     """Without the early plan, seq_lens may be written by the kernel right
     before the decode (a fill); the queries may always be.  With the early
-    plan the lengths come from a host copy and only q is rewritten."""
+    plan (either level) the lengths come from a host copy and only q is
+    rewritten."""
     S, Hq, Hkv, d = 6, 12, 2, 128
     inp = workloads.decode_inputs(S, Hq, Hkv, d, seed=90, len_lo=700, len_hi=700)
     dv = {k: (t.to(DEV) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
@@ -118,3 +119,63 @@ def test_chained_fusions_consume_the_previous_output():
     y_ref = attn.fused_swiglu(torch.cat([a2, a1], dim=1).contiguous())
     torch.cuda.synchronize()
     assert torch.equal(out1, a1) and torch.equal(out2, a2) and torch.equal(res, r) and torch.equal(y, y_ref)
+
+
+def _last_blocks_first(inp):
+    """The same decode inputs with the physical blocks relabelled so that
+    block b is the last block of sequence b: the last blocks of all the
+    sequences form one contiguous slice of each cache."""
+    table = inp["block_table"].clone()
+    lens = inp["seq_lens"].tolist()
+    nb = inp["k_cache"].shape[0]
+    last = [int(table[b, (L + 15) // 16 - 1]) for b, L in enumerate(lens)]
+    rest = [i for i in range(nb) if i not in set(last)]
+    order = last + rest                                # new id -> old id
+    new_id = torch.empty(nb, dtype=torch.int64)
+    new_id[torch.tensor(order)] = torch.arange(nb)
+    valid = table >= 0
+    table[valid] = new_id[table[valid].long()].to(torch.int32)
+    return dict(inp, block_table=table, k_cache=inp["k_cache"][order].contiguous(),
+                v_cache=inp["v_cache"][order].contiguous())
+
+
+@pytest.mark.parametrize("early", [0, 1, 2])
+def test_decode_sees_last_blocks_written_just_before(early):
+    """The newest token's block of every sequence (its last block) may be
+    written by the kernel right before the decode at every early-plan
+    level.  Here two residual-add kernels, launched as programmatic
+    dependents that let their own dependents start early, rewrite the last
+    K and V blocks of all 40 sequences in place just before the call; with
+    lengths of 1 to 300 tokens every CTA's first blocks include last blocks,
+    which the early stream of level 2 must leave for after the wait."""
+    S, Hq, Hkv, d = 40, 12, 2, 128
+    inp = _last_blocks_first(workloads.decode_inputs(S, Hq, Hkv, d, seed=97, len_lo=1, len_hi=300))
+    g = torch.Generator().manual_seed(98)
+    rows = S * Hkv * 16
+    # Large changes to the keys move the scores; V changes by half its own
+    # scale, so |O| stays in the range of the other decode cases (a bf16 ulp
+    # of 8 is 0.0625 by itself, beyond the absolute bound).
+    xk = (4 * torch.randn(rows, d, generator=g)).to(torch.bfloat16).to(DEV)
+    xv = (0.5 * torch.randn(rows, d, generator=g)).to(torch.bfloat16).to(DEV)
+    w = torch.ones(d, dtype=torch.bfloat16, device=DEV)
+    dv = {k: (t.to(DEV) if isinstance(t, torch.Tensor) else t) for k, t in inp.items()}
+    try:
+        attn.set_decode_early_plan(early)
+        for _ in range(2):                            # a warm call, then the checked one
+            kc, vc = dv["k_cache"].clone(), dv["v_cache"].clone()
+            torch.cuda.synchronize()
+            attn.fused_add_rmsnorm(xk, kc[:S].view(rows, d), w)
+            attn.fused_add_rmsnorm(xv, vc[:S].view(rows, d), w)
+            o, lse = attn.attn_decode_paged(dv["q"], kc, vc, dv["block_table"], dv["seq_lens"], scale=0.1)
+            torch.cuda.synchronize()
+    finally:
+        attn.set_decode_early_plan(0)
+    assert attn.device_status() == 0
+    kc64, vc64 = to64(kc.cpu()), to64(vc.cpu())
+    args = (to64(inp["q"]),)
+    tail = (inp["block_table"].numpy(), inp["seq_lens"].numpy(), 0.1)
+    o_new, lse_new = oracle.decode_paged(*args, kc64, vc64, *tail)
+    o_old, _ = oracle.decode_paged(*args, to64(inp["k_cache"]), to64(inp["v_cache"]), *tail)
+    # The rewrite moves the outputs far beyond the tolerance, so a stale read would show.
+    assert abs(o_new - o_old).max() > 0.5
+    assert_attn_close(o, lse, o_new, lse_new, what="decode after last blocks rewritten, early %d" % early)
