@@ -76,23 +76,30 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;        // lazy-rescale threshold, log2 units
 
-template <int D>
+// SUMV (d = 64 with contiguous K/V): the row sums of P come from the tensor
+// core.  Every V stage gets a second 64-column chunk, written once, whose
+// first column is all ones, and P V runs with N = d + 16: columns d .. d+15
+// of O_X then hold P times that column, the row sums of the bf16 P that P V
+// uses, at no extra MMA instruction (three stages instead of four make room).
+template <int D, bool SUMV = false>
 struct FwdLayout {
   static constexpr int kChunks = D / 64;                 // 128-byte swizzle atoms per row
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStages = (D == 128) ? 2 : SUMV ? 3 : 4;
   static constexpr int kQTile = kBM * D * 2;
   static constexpr int kKV = kBN * D * 2;
   static constexpr int kQChunk = kBM * 128;              // one 64-column box of a Q tile
   static constexpr int kKVChunk = kBN * 128;
+  static constexpr int kVStage = SUMV ? kKV + kKVChunk : kKV;   // V stage stride (+ the ones chunk)
+  static constexpr int kNPV = SUMV ? D + 16 : D;         // N of the P V MMAs
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTiles * kQTile;
   static constexpr int kOffV = kOffK + kStages * kKV;
-  static constexpr int kOffBar = kOffV + kStages * kKV;
+  static constexpr int kOffBar = kOffV + kStages * kVStage;
   static constexpr int kOffCtx = kOffBar + 512;          // paged: ctx_b of each sequence
   static constexpr int kOffOrder = kOffCtx + 4 * 256;    // paged: (b << 16 | qblk) of each cost rank
   static constexpr int kSmem = kOffOrder + 4 * 2048 + 1024;   // + alignment slack
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
-  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  static constexpr uint32_t kColO0 = 256, kColO1 = SUMV ? 384 : 256 + D;
 };
 
 struct FwdBarriers {
@@ -136,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_sm103_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv, const FwdParams p) {
-  using L = FwdLayout<D>;
+  constexpr bool SUMV = D == 64 && !PAGED;
+  using L = FwdLayout<D, SUMV>;
   extern __shared__ uint8_t smem_raw[];
   // Aligned through an integer round trip (the pointer becomes generic):
   // measured faster for this kernel than smem_align1024.
@@ -228,6 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(&bar->tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  if constexpr (SUMV) {
+    // The ones chunk of every V stage: in key row r, bf16 1.0 in its column
+    // 0, whose 16-byte piece sits at piece 0 ^ (r mod 8) of the row's 128
+    // bytes (the TMA's 128-byte swizzle); zeros elsewhere.
+    for (int i = threadIdx.x; i < L::kStages * L::kKVChunk / 4; i += kThreads) {
+      const int st = i / (L::kKVChunk / 4), k = i % (L::kKVChunk / 4);
+      const int r = k / 32, w = k % 32;
+      reinterpret_cast<uint32_t*>(smem + L::kOffV + st * L::kVStage + L::kKV)[k] =
+          (w == (r & 7) * 4) ? 0x3F80u : 0u;
+    }
+    fence_proxy_async_smem();
+  }
   // Launched as a programmatic dependent: the set-up above overlaps the end
   // of the kernel before this one in the stream; nothing in global memory
   // is read or written before that kernel has finished.
@@ -313,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           if (!(ok = mbar_wait(smem_addr(&bar->v_empty[st]), ph ^ 1, wc))) break;
-          load_kv(sV + st * L::kKV, &tv, smem_addr(&bar->v_full[st]));
+          load_kv(sV + st * L::kVStage, &tv, smem_addr(&bar->v_full[st]));
           ++v_issued;
         }
         kv_issued += u.nB;
@@ -337,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- MMA issuer
     {
       constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, L::kNPV, true);
       constexpr int kSteps = D / 16;               // MMAs in an S group (K = d)
       constexpr int kPSteps = kBN / 16;            // MMAs in a PV group (K = keys)
       const uint32_t kF = smem_addr(&bar->k_full[0]);
@@ -382,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto group_pv = [&](int x, int jj) {
         const int st = (g0 + jj) % L::kStages;
-        const uint32_t vbase = sV + st * L::kKV;
+        const uint32_t vbase = sV + st * L::kVStage;
         const uint32_t aP = tmem + (x ? L::kColS1 : L::kColS0);
         const uint32_t dO = tmem + (x ? L::kColO1 : L::kColO0);
 #pragma unroll
@@ -627,8 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Numerators p = 2^(s * scale * log2 e - m), two lanes per instruction
       // for the scale and the sums.  Two denominators: `lr` sums the
       // bf16-rounded numerators that P V uses, so O / lr weights every value
-      // row by exactly the factor it got; `l` sums the fp32 numerators and
-      // gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
+      // row by exactly the factor it got (with SUMV the tensor core forms
+      // this sum in column d of O_X and the loop leaves it out); `l` sums the
+      // fp32 numerators and gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
       // 2c+1 in column c), the first half while the second is computed.
       float lt, lrt;                               // this tile's two sums
       auto numerators = [&]() {
@@ -647,8 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2(x0), p1 = ex2(x1);
             const uint32_t w = pack_bf16x2(p0, p1);
             accE[c & 3] = f2_add(accE[c & 3], f2_pack(p0, p1));
-            accR[(c & 1) * 2] = add_bf16lo_f32(w, accR[(c & 1) * 2]);
-            accR[(c & 1) * 2 + 1] = add_bf16hi_f32(w, accR[(c & 1) * 2 + 1]);
+            if constexpr (!SUMV) {
+              accR[(c & 1) * 2] = add_bf16lo_f32(w, accR[(c & 1) * 2]);
+              accR[(c & 1) * 2 + 1] = add_bf16hi_f32(w, accR[(c & 1) * 2 + 1]);
+            }
             pk[c] = w;
           }
           ATTN47_TMEM_ST32(tl + colS + half * 32, pk);
@@ -671,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = m_new;
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < (SUMV ? D + 32 : D); c0 += 32) {   // SUMV: the row sums too
             uint32_t o[32];
             ATTN47_TMEM_LD32(tl + colO + c0, o);
             ATTN47_TMEM_LD_WAIT(o);
@@ -719,7 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok && mbar_wait_warp(smem_addr(&bar->o_done[x]), static_cast<uint32_t>(units & 1), wc)) {
       tc_fence_after();
-      const float inv_l = 1.f / lr;
+      float lsum = lr;
+      if constexpr (SUMV) {
+        uint32_t rs[32];
+        ATTN47_TMEM_LD32(tl + colO + D, rs);
+        ATTN47_TMEM_LD_WAIT(rs);
+        lsum = __uint_as_float(rs[0]);
+      }
+      const float inv_l = 1.f / lsum;
       const bool in_range = qrow < p.N;
       __nv_bfloat16* orow =
           reinterpret_cast<__nv_bfloat16*>(p.o) + (static_cast<size_t>(zq) * p.N + qrow) * D;
@@ -758,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL, bool PAGED, bool SORTED = false>
 cudaError_t launch_t(const FwdLaunch& a) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, D == 64 && !PAGED>;
   auto kern = attn_fwd_sm103_kernel<D, CAUSAL, PAGED, SORTED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
   if (e != cudaSuccess) return e;
