@@ -371,7 +371,7 @@ def fwd_config_table(attn, device, steps, peak):
 
 
 def bwd_measurement(attn, device, steps, peak):
-    """attn_bwd on the qwen_gqa_prefill workload (all three kernels per call),
+    """attn_bwd on the qwen_gqa_prefill workload (both kernels per call),
     CUDA events over `steps` calls after 3 warm-ups.  FLOPs: 2.5 x the forward
     count (five matmuls of the forward's tile sizes against its two)."""
     c = workloads.PREFILL_CONFIGS[FWD_CFG]
