@@ -70,11 +70,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CSRC = os.path.join(ROOT, "exact_attention_47_gb300", "csrc")
 TRAFFIC = {
     # median read + median write of 3 launches
-    "fwd": {"bytes": 67193088 + 5278720, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
-            "sha256": "050cf2db2a451483c3e8e518be7af2e3320dcb6db5b07f6956d2276276d7949a"},
+    "fwd": {"bytes": 67196160 + 5156352, "sources": ("fwd_sm103.cu", "fwd_sm103.h", "ptx.cuh"),
+            "sha256": "c061cce87aac37cddee53f431a14b87c1d506ad4be6b6457a2c5d3c8dc08a1fe"},
     # decode kernel (split parts merged inside it), median read + median write of 3 launches
-    "dec": {"bytes": 132365312 + 165376, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
-            "sha256": "0263f5ed5168d29bf135158af364813e2328c6ac16c8870a324f05cfe2371f8b"},
+    "dec": {"bytes": 132366848 + 414976, "sources": ("decode_sm103.cu", "decode_sm103.h", "ptx.cuh"),
+            "sha256": "f99b6fe8bb0649fd0f754ee35830d2875c82b20eee2a8b35250d418badad3f9b"},
 }
 
 

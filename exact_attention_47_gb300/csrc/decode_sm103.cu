@@ -36,7 +36,9 @@
 // (griddepcontrol.wait) before touching anything it may write.  With the
 // early plan on, the wait comes after the split plan and the first table
 // translations, which then read seq_lens and the block table before the
-// preceding kernel has finished.
+// preceding kernel has finished; at level 2 the producer also issues the
+// K/V copies of the ring's first fill before the wait, leaving out each
+// sequence's last block (where a decode step appends its newest token).
 #include <cuda_runtime.h>
 
 #include "decode_sm103.h"

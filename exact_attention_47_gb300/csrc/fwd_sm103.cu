@@ -16,7 +16,9 @@
 //   warps 10-11 idle (they complete the third warpgroup for setmaxnreg);
 //               in paged mode they gather the K and V tiles
 // Tensor memory: S_A, S_B (128 fp32 columns each), O_A, O_B (d columns
-// each).  After reading S_X, the softmax writes P_X (bf16, two per column)
+// each; at d = 64 with contiguous K/V, d + 16, the extra columns holding the
+// row sums of P that P V forms against a ones column beside V).  After
+// reading S_X, the softmax writes P_X (bf16, two per column)
 // over the first 64 columns of S_X and the MMA reads it from there (A
 // operand in TMEM), so P never touches shared memory.  The tensor core runs
 // ... PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) ... in issue order, so while one
@@ -649,8 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // bf16-rounded numerators that P V uses, so O / lr weights every value
       // row by exactly the factor it got (with SUMV the tensor core forms
       // this sum in column d of O_X and the loop leaves it out); `l` sums the
-      // fp32 numerators and gives the LSE.  P_X goes over the first 64 columns of S_X (keys 2c,
-      // 2c+1 in column c), the first half while the second is computed.
+      // fp32 numerators and gives the LSE.  P_X goes over the first 64
+      // columns of S_X (keys 2c, 2c+1 in column c), the first half while the
+      // second is computed.
       float lt, lrt;                               // this tile's two sums
       auto numerators = [&]() {
         const uint64_t sc2 = f2_pack(sl2, sl2);
