@@ -292,6 +292,38 @@ def test_early_plan_gives_identical_bits():
     assert_attn_close(*res[2][2], *ref(inps[2], scale), what="early plan, third call")
 
 
+@pytest.mark.parametrize("S,Hq,Hkv,d,lo,hi", [
+    (48, 16, 1, 128, 1, 400),     # 16 query heads per KV head: the 14-stage ring
+    (40, 8, 8, 64, 1, 300),       # d = 64, one query head per KV head
+    (6, 12, 2, 128, 3000, 9000),  # few long sequences: every CTA inside one run
+], ids=["G16", "d64", "long"])
+def test_early_stream_levels_give_identical_bits(S, Hq, Hkv, d, lo, hi):
+    """Every level of the early plan gives the same bits on the other kernel
+    instances too: short sequences put last blocks of sequences among the
+    first blocks of most CTAs (which the early stream leaves for after the
+    wait), long ones give CTAs whose first blocks are all early."""
+    inp = workloads.decode_inputs(S, Hq, Hkv, d, seed=60 + Hq + d, len_lo=lo, len_hi=hi)
+    dv = to_dev(inp)
+    scale = workloads.default_scale(d)
+    ws = torch.empty(attn.attn_decode_paged_workspace_size(S, Hq, d, dv["block_table"].shape[1]),
+                     dtype=torch.uint8, device=DEV)
+    res = {}
+    try:
+        for early in (0, 1, 2):
+            attn.set_decode_early_plan(early)
+            o, lse = _outs(dv)
+            for _ in range(2):                         # back to back: the second overlaps the first
+                _call(dv, scale, o, lse, ws)
+            torch.cuda.synchronize()
+            res[early] = (o, lse)
+    finally:
+        attn.set_decode_early_plan(0)
+    assert attn.device_status() == 0
+    for level in (1, 2):
+        assert torch.equal(res[0][0], res[level][0]) and torch.equal(res[0][1], res[level][1])
+    assert_attn_close(*res[2], *ref(inp, scale), what="early stream, S %d Hq %d Hkv %d d %d" % (S, Hq, Hkv, d))
+
+
 def test_long_sequences_split_into_many_parts():
     """Eight 16384-token sequences over one wave: every (sequence, KV head)
     run is split over about ten CTAs, so the part that arrives last merges
