@@ -92,6 +92,22 @@ def test_scales_and_wide_logits(scale, v_std, d, causal):
                       what="d %d, causal %d, scale %g, V std %g" % (d, causal, scale, v_std))
 
 
+@pytest.mark.parametrize("d,causal", [(64, True), (64, False), (128, True), (128, False)])
+def test_score_jump_forces_rescale_and_redo(d, causal):
+    """Keys 256..383 scaled by 8 (exactly, in bf16): their scores exceed the
+    earlier tiles' by about 250 in log2 units, so the numerators formed with
+    the stabiliser in use overflow, the tile is redone with its own maximum,
+    and O and both sums are rescaled by a factor that underflows to zero;
+    rows that cannot see those keys (causal, rows < 256) keep the lazy
+    stabiliser throughout.  At d = 64 the rescale includes the row-sum
+    column the tensor core fills."""
+    q, k, v = workloads.prefill_inputs(1, 2, 2, 512, d, seed=17)
+    k = k.clone()
+    k[:, :, 256:384] = (k[:, :, 256:384].float() * 8).to(torch.bfloat16)
+    o, lse = run(q, k, v, causal, 1.0)
+    assert_attn_close(o, lse, *ref(q, k, v, causal, 1.0), what="score jump, d %d, causal %d" % (d, causal))
+
+
 def test_gpt2_small_config_all_rows():
     c = workloads.PREFILL_CONFIGS["gpt2_small"]
     q, k, v = workloads.prefill_inputs(c["B"], c["Hq"], c["Hkv"], c["N"], c["d"], c["seed"])
