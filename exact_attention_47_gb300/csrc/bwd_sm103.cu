@@ -12,7 +12,9 @@
 //
 // Two kernels, in stream order:
 //   attn_bwd_rowdot_kernel     D and lse * log2(e) per query row (HBM-bound)
-//   attn_bwd_kernel            one tile per CTA, of one of two kinds:
+//   attn_bwd_kernel            one tile per CTA, of one of two kinds (one
+//                              grid of both at d = 128, a grid of each at
+//                              d = 64):
 //     dK/dV: one 128-key tile, looping over the query tiles of every query
 //            head of its group;
 //     dQ:    one 128-row query tile, looping over K/V.
@@ -643,26 +645,42 @@ __device__ __forceinline__ void bwd_dkdv_tile(const CUtensorMap& tq, const CUten
   }
 }
 
-// ------------------------------------------------------------ one launch
+// ------------------------------------------------------------ launches
 // The dK/dV and dQ work are independent (both read only the row-dot pass's
-// output), so one grid carries both: the dK/dV key tiles first (the largest
-// units: a key tile of a KV head covers the query tiles of all its query
-// heads), then the dQ query tiles, heaviest first.  The many small dQ units
-// fill the SMs that the dK/dV units' uneven causal sizes leave idle.
-template <int D, bool CAUSAL>
+// output).  At d = 128 one grid carries both (KIND 0): the dK/dV key tiles
+// first (the largest units: a key tile of a KV head covers the query tiles
+// of all its query heads), then the dQ query tiles, heaviest first; the
+// many small dQ units fill the SMs that the dK/dV units' uneven causal sizes
+// leave idle.  At d = 64 the units are short and the two kinds run as two
+// grids, dQ (KIND 1) then dK/dV (KIND 2), which measured faster there.
+template <int D, bool CAUSAL, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const BwdParams p) {
-  const int n_kv_units = (p.N + kTile - 1) / kTile * p.bh_kv;
   const int unit = static_cast<int>(blockIdx.x);
-  if (unit < n_kv_units) bwd_dkdv_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit);
-  else bwd_dq_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit - n_kv_units);
+  if constexpr (KIND == 1) {
+    bwd_dq_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit);
+  } else if constexpr (KIND == 2) {
+    bwd_dkdv_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit);
+  } else {
+    const int n_kv_units = (p.N + kTile - 1) / kTile * p.bh_kv;
+    if (unit < n_kv_units) bwd_dkdv_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit);
+    else bwd_dq_tile<D, CAUSAL>(tq, tk, tv, tdo, p, unit - n_kv_units);
+  }
+}
+
+template <int D, bool CAUSAL, int KIND>
+cudaError_t launch_tiles(const BwdLaunch& a, const BwdParams& p, unsigned units) {
+  using L = BwdLayout<D>;
+  auto k = attn_bwd_kernel<D, CAUSAL, KIND>;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3(units), dim3(kThreads), L::kSmem, a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
-  using L = BwdLayout<D>;
   const int nq = (a.N + kTile - 1) / kTile;
   {
     const long long rows = static_cast<long long>(p.bh_q) * p.n_pad;
@@ -672,11 +690,13 @@ cudaError_t launch_t(const BwdLaunch& a, BwdParams p) {
                                      dim3(256), 0, a.stream, p);
     if (e != cudaSuccess) return e;
   }
-  auto k = attn_bwd_kernel<D, CAUSAL>;
-  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmem);
-  if (e != cudaSuccess) return e;
-  const unsigned units = static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv + p.bh_q);
-  return launch_pdl(k, dim3(units), dim3(kThreads), L::kSmem, a.stream, *a.tq, *a.tk, *a.tv, *a.tdo, p);
+  if constexpr (D == 128) {
+    return launch_tiles<D, CAUSAL, 0>(a, p, static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv + p.bh_q));
+  } else {
+    const cudaError_t e = launch_tiles<D, CAUSAL, 1>(a, p, static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_q));
+    if (e != cudaSuccess) return e;
+    return launch_tiles<D, CAUSAL, 2>(a, p, static_cast<unsigned>(nq) * static_cast<unsigned>(p.bh_kv));
+  }
 }
 
 }  // namespace
